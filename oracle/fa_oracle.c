@@ -1,0 +1,239 @@
+/*
+ * fa_oracle.c — plain, slow, obviously correct CPU oracle for the non-causal
+ * scaled-dot-product attention forward with row log-sum-exp.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path links, loads or calls
+ * this file: only the tests, the smoke check and the benchmark's CPU-baseline /
+ * reference arm do.  It shares no code, header, table or helper with the CUDA
+ * library.
+ *
+ * What it computes (the plain definition, in fp64 throughout):
+ *
+ *   s_ij   = scale * sum_d q[b,h,i,d] * k[b,h,j,d]   (+ mask[b,j] if a mask is given)
+ *   m_i    = max_j s_ij
+ *   l_i    = sum_j exp(s_ij - m_i)
+ *   O[i,:] = sum_j exp(s_ij - m_i) * v[b,h,j,:] / l_i
+ *   LSE_i  = m_i + ln(l_i)
+ *
+ * Sources, by page and section:
+ *  - "算子加速：注意力、编译与融合" (anrans.github.io ai-infra-handbooks, perf/kernels),
+ *    section "注意力：从O(N²)显存到分块", worked example function `naive`:
+ *    scores = q k^T / sqrt(D), softmax over the key axis, times v.
+ *  - "FlashAttention原理与工业实战" (sheratonhq.com), §2.1: a mask entry of
+ *    "ignore" becomes -inf before the softmax.
+ *  - "Step 3.7 Flash" SD1.5 case study (pwwt.cn), §2.3: the scores are scaled
+ *    first and the additive mask is added after the scale (large negative for
+ *    ignored positions).
+ *  - "FlashAttention原理与工业实战" §2.3 kernel signature: the forward also
+ *    writes a per-row Lse; its base is not stated, the natural log is used.
+ *
+ * Readings where the pages are silent:
+ *  - the mask is an additive fp32 key-padding mask of shape [B, Nk], broadcast
+ *    over heads and query rows; it is not multiplied by `scale`;
+ *  - a row whose every score is -inf (all keys masked) gives O = 0 and
+ *    LSE = -inf;
+ *  - the softmax is two-pass over a materialised fp64 score row (max, then
+ *    exp/sum), which is exactly the textbook definition.
+ *
+ * Inputs are fp32 or raw bf16 bit patterns (uint16), widened exactly to fp64.
+ * Layout: q [B,H,Nq,D], k and v [B,H,Nk,D], contiguous row-major.
+ * Outputs are fp64: O [B,H,Nq,D] (or [B,H,nrows,D] in sampled mode), LSE
+ * [B,H,Nq] (or [B,H,nrows]).
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_DTYPE_F32 0
+#define ORACLE_DTYPE_BF16 1
+
+/* Widen one input element to fp64.  bf16 is the upper half of an fp32. */
+static double load_elem(const void* base, int dtype, int64_t idx) {
+    if (dtype == ORACLE_DTYPE_BF16) {
+        uint16_t bits = ((const uint16_t*)base)[idx];
+        uint32_t wide = ((uint32_t)bits) << 16;
+        float f;
+        memcpy(&f, &wide, sizeof f);
+        return (double)f;
+    }
+    return (double)((const float*)base)[idx];
+}
+
+typedef struct {
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* mask; /* [B, Nk] or NULL */
+    int dtype;
+    int B, H, Nq, Nk, D;
+    double scale;
+    const int64_t* rows; /* NULL: every row; else [B*H, nrows] query indices */
+    int nrows;
+    double* out;
+    double* lse;
+    int64_t total_items;          /* number of (head, row) items */
+    int64_t next_item;            /* shared work counter */
+} oracle_job;
+
+/* One query row of one head: materialise the score row, then softmax, then the
+ * weighted sum of V rows.  s and p are scratch buffers of length Nk. */
+static void attend_one_row(const oracle_job* job, int64_t bh, int64_t i, double* o_row,
+                           double* lse_out, double* s, double* p) {
+    const int Nk = job->Nk, D = job->D, Nq = job->Nq;
+    const int64_t b = bh / job->H;
+    const int64_t q_base = (bh * Nq + i) * D;
+    const int64_t kv_base = bh * (int64_t)Nk * D;
+
+    /* s_ij = scale * (q_i . k_j) + mask_bj */
+    for (int j = 0; j < Nk; ++j) {
+        double dot = 0.0;
+        for (int d = 0; d < D; ++d) {
+            dot += load_elem(job->q, job->dtype, q_base + d) *
+                   load_elem(job->k, job->dtype, kv_base + (int64_t)j * D + d);
+        }
+        double sij = job->scale * dot;
+        if (job->mask) sij += (double)job->mask[b * Nk + j];
+        s[j] = sij;
+    }
+
+    /* m_i = max_j s_ij */
+    double m = -INFINITY;
+    for (int j = 0; j < Nk; ++j)
+        if (s[j] > m) m = s[j];
+
+    if (m == -INFINITY) { /* every key masked */
+        for (int d = 0; d < D; ++d) o_row[d] = 0.0;
+        *lse_out = -INFINITY;
+        return;
+    }
+
+    /* p_ij = exp(s_ij - m_i), l_i = sum_j p_ij */
+    double l = 0.0;
+    for (int j = 0; j < Nk; ++j) {
+        p[j] = exp(s[j] - m);
+        l += p[j];
+    }
+
+    /* O_i = sum_j p_ij v_j / l_i */
+    for (int d = 0; d < D; ++d) o_row[d] = 0.0;
+    for (int j = 0; j < Nk; ++j) {
+        for (int d = 0; d < D; ++d)
+            o_row[d] += p[j] * load_elem(job->v, job->dtype, kv_base + (int64_t)j * D + d);
+    }
+    for (int d = 0; d < D; ++d) o_row[d] /= l;
+
+    *lse_out = m + log(l);
+}
+
+static void* worker(void* arg) {
+    oracle_job* job = (oracle_job*)arg;
+    double* s = (double*)malloc(sizeof(double) * (size_t)job->Nk);
+    double* p = (double*)malloc(sizeof(double) * (size_t)job->Nk);
+    if (!s || !p) {
+        free(s);
+        free(p);
+        return (void*)1;
+    }
+    const int64_t per_head = job->rows ? job->nrows : job->Nq;
+    for (;;) {
+        int64_t item = __atomic_fetch_add(&job->next_item, 1, __ATOMIC_RELAXED);
+        if (item >= job->total_items) break;
+        int64_t bh = item / per_head;
+        int64_t r = item % per_head;
+        int64_t i = job->rows ? job->rows[bh * job->nrows + r] : r;
+        attend_one_row(job, bh, i, job->out + item * job->D, job->lse + item, s, p);
+    }
+    free(s);
+    free(p);
+    return NULL;
+}
+
+static int run_job(oracle_job* job, int nthreads) {
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 1024) nthreads = 1024;
+    if (job->total_items < nthreads) nthreads = (int)(job->total_items > 0 ? job->total_items : 1);
+    pthread_t* tids = (pthread_t*)malloc(sizeof(pthread_t) * (size_t)nthreads);
+    if (!tids) return 2;
+    int started = 0, failed = 0;
+    for (int t = 0; t < nthreads; ++t) {
+        if (pthread_create(&tids[t], NULL, worker, job) != 0) break;
+        ++started;
+    }
+    if (started == 0) { /* run inline */
+        if (worker(job) != NULL) failed = 1;
+    }
+    for (int t = 0; t < started; ++t) {
+        void* rv = NULL;
+        pthread_join(tids[t], &rv);
+        if (rv != NULL) failed = 1;
+    }
+    free(tids);
+    return failed ? 2 : 0;
+}
+
+static int check_shape(int B, int H, int Nq, int Nk, int D) {
+    return (B >= 1 && H >= 1 && Nq >= 1 && Nk >= 1 && D >= 1) ? 0 : 1;
+}
+
+/* Full forward: O [B,H,Nq,D] and LSE [B,H,Nq], both fp64.
+ * Returns 0 on success, 1 on a bad shape or pointer, 2 on an allocation or
+ * thread failure. */
+int fa_oracle_fwd(const void* q, const void* k, const void* v, const float* mask, int dtype,
+                  double* out, double* lse, int B, int H, int Nq, int Nk, int D, double scale,
+                  int nthreads) {
+    if (!q || !k || !v || !out || !lse || check_shape(B, H, Nq, Nk, D)) return 1;
+    if (dtype != ORACLE_DTYPE_F32 && dtype != ORACLE_DTYPE_BF16) return 1;
+    oracle_job job = {q, k, v, mask, dtype, B, H, Nq, Nk, D, scale, NULL, 0, out, lse,
+                      (int64_t)B * H * Nq, 0};
+    return run_job(&job, nthreads);
+}
+
+/* Sampled forward: for each head bh, the query rows rows[bh*nrows + r].
+ * O [B,H,nrows,D] and LSE [B,H,nrows], fp64. */
+int fa_oracle_rows(const void* q, const void* k, const void* v, const float* mask, int dtype,
+                   const int64_t* rows, int nrows, double* out, double* lse, int B, int H, int Nq,
+                   int Nk, int D, double scale, int nthreads) {
+    if (!q || !k || !v || !out || !lse || !rows || nrows < 1 || check_shape(B, H, Nq, Nk, D))
+        return 1;
+    if (dtype != ORACLE_DTYPE_F32 && dtype != ORACLE_DTYPE_BF16) return 1;
+    for (int64_t t = 0; t < (int64_t)B * H * nrows; ++t)
+        if (rows[t] < 0 || rows[t] >= Nq) return 1;
+    oracle_job job = {q, k, v, mask, dtype, B, H, Nq, Nk, D, scale, rows, nrows, out, lse,
+                      (int64_t)B * H * nrows, 0};
+    return run_job(&job, nthreads);
+}
+
+/* The softmax probabilities of one row (b, h, i): p_j = exp(s_ij - m_i) / l_i,
+ * written to probs[Nk].  A fully masked row gives all zeros.  Used to check
+ * that each row of the attention matrix is a probability distribution. */
+int fa_oracle_probs(const void* q, const void* k, const float* mask, int dtype, int b, int h,
+                    int i, double* probs, int B, int H, int Nq, int Nk, int D, double scale) {
+    if (!q || !k || !probs || check_shape(B, H, Nq, Nk, D)) return 1;
+    if (b < 0 || b >= B || h < 0 || h >= H || i < 0 || i >= Nq) return 1;
+    const int64_t bh = (int64_t)b * H + h;
+    const int64_t q_base = (bh * Nq + i) * D;
+    const int64_t k_base = bh * (int64_t)Nk * D;
+    double m = -INFINITY;
+    for (int j = 0; j < Nk; ++j) {
+        double dot = 0.0;
+        for (int d = 0; d < D; ++d)
+            dot += load_elem(q, dtype, q_base + d) * load_elem(k, dtype, k_base + (int64_t)j * D + d);
+        double sij = scale * dot;
+        if (mask) sij += (double)mask[(int64_t)b * Nk + j];
+        probs[j] = sij;
+        if (sij > m) m = sij;
+    }
+    if (m == -INFINITY) {
+        for (int j = 0; j < Nk; ++j) probs[j] = 0.0;
+        return 0;
+    }
+    double l = 0.0;
+    for (int j = 0; j < Nk; ++j) {
+        probs[j] = exp(probs[j] - m);
+        l += probs[j];
+    }
+    for (int j = 0; j < Nk; ++j) probs[j] /= l;
+    return 0;
+}
