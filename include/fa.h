@@ -1,0 +1,89 @@
+/*
+ * fa.h — C ABI of the GB300 (sm_103a) FlashAttention-style attention forward.
+ *
+ * Operation (non-causal scaled-dot-product attention with row log-sum-exp):
+ *
+ *   S = scale * Q K^T (+ mask broadcast over heads and query rows)
+ *   O = softmax_row(S) V,   LSE_i = ln sum_j exp(S_ij)
+ *
+ * computed block by block with an online softmax (running row max m, running
+ * denominator l, rescaled accumulator), so the Nq x Nk score matrix never
+ * reaches device memory.  Sources:
+ *  - "算子加速：注意力、编译与融合" (anrans.github.io ai-infra-handbooks, perf/kernels),
+ *    section "注意力：从O(N²)显存到分块": the figure (per K/V block: S_ij = Q_i K_j^T,
+ *    update m and l, O_i <- O_i e^(m_old - m) + P V_j, only O_i is written
+ *    back) and the `blocked` worked example (the m / l / acc recurrence);
+ *  - "FlashAttention原理与工业实战" (sheratonhq.com) §2.3: the forward kernel
+ *    writes Out and a per-row Lse; §4.3: inputs must be contiguous [B,H,N,D];
+ *  - "Step 3.7 Flash" (pwwt.cn) §2.3 and §3.1: scale first, then add the
+ *    additive attention mask; non-causal (is_causal=False).
+ *
+ * All functions are thread-safe.  The library allocates no device memory.
+ */
+#ifndef UNET_FA_FWD_GB300_FA_H
+#define UNET_FA_FWD_GB300_FA_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes returned by every entry point. */
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARGUMENT = 1, /* NULL pointer, bad size, misaligned or overlapping buffer, non-finite scale */
+    FA_ERR_UNSUPPORTED = 2,      /* head dimension D not in {32, 64, 128}; device not sm_103 */
+    FA_ERR_CUDA = 3,             /* a CUDA runtime/driver call failed (launch, attribute, tensor map) */
+    FA_ERR_TIMEOUT = 4           /* a kernel wait ran past its time limit (read with fa_read_device_status) */
+} fa_status;
+
+/*
+ * fa_fwd — attention forward on the GPU.
+ *
+ *   q     device pointer, bf16 [B, H, Nq, D], contiguous row-major
+ *   k, v  device pointers, bf16 [B, H, Nk, D], contiguous row-major
+ *   mask  device pointer to an fp32 additive key mask [B, Nk] (0 = keep,
+ *         -inf = ignore; any finite value is added to the scaled score), or
+ *         NULL for no mask.  Broadcast over heads and query rows.
+ *   out   device pointer, bf16 [B, H, Nq, D]: O
+ *   lse   device pointer, fp32 [B, H, Nq]: natural-log row log-sum-exp of the
+ *         scaled, masked scores
+ *   B, H, Nq, Nk  >= 1;  D in {32, 64, 128}
+ *   scale finite; multiplies Q K^T before the mask is added
+ *   stream  cudaStream_t (as void*), NULL = the legacy default stream
+ *
+ * A row whose keys are all masked gives O = 0 and LSE = -inf.
+ *
+ * Ownership: the caller owns every buffer; nothing is retained after the call
+ * returns except a host-side cache of TMA descriptors keyed by pointer and
+ * shape.  Every pointer must be 16-byte aligned (a TMA requirement); out and
+ * lse must not overlap q, k, v, mask or each other.
+ *
+ * Errors: arguments are validated before any CUDA call; an invalid call
+ * returns FA_ERR_INVALID_ARGUMENT or FA_ERR_UNSUPPORTED and launches nothing.
+ * FA_ERR_CUDA means a launch or set-up call failed.  FA_OK means the kernel
+ * was enqueued on `stream` (the call is asynchronous); a kernel that ran out
+ * of time on an internal wait records FA_ERR_TIMEOUT in the device status
+ * word (see fa_read_device_status) and exits without hanging.
+ */
+int fa_fwd(const void* q, const void* k, const void* v, const float* mask, void* out, float* lse,
+           int B, int H, int Nq, int Nk, int D, float scale, void* stream);
+
+/*
+ * fa_read_device_status — read, and reset to FA_OK, the status word that
+ * kernels on the current device write when an internal wait times out.
+ * Synchronises `stream` first.  Writes FA_OK or FA_ERR_TIMEOUT to *status.
+ * Returns FA_OK, FA_ERR_INVALID_ARGUMENT (status NULL) or FA_ERR_CUDA.
+ */
+int fa_read_device_status(void* stream, int* status);
+
+/* Human-readable name of a status code (static storage; never NULL). */
+const char* fa_status_string(int status);
+
+/* Library version string, e.g. "unet_fa_fwd_gb300 0.1.0 sm_103a" (static storage). */
+const char* fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* UNET_FA_FWD_GB300_FA_H */

@@ -1,0 +1,80 @@
+"""The C-ABI library loads on a machine without a GPU, exports every function
+include/fa.h declares, and validates arguments before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import unet_fa_fwd_gb300 as fa
+from unet_fa_fwd_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    names = []
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if h.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", h), encoding="utf-8").read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"^[A-Za-z_][\w \*]*?\b(fa_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return fa.load_library()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared()
+    assert {"fa_fwd", "fa_status_string", "fa_version", "fa_read_device_status"} <= set(names)
+    raw = ctypes.CDLL(_build.LIB)
+    for n in names:
+        assert hasattr(raw, n), n
+
+
+def test_strings(lib):
+    assert fa.version().startswith("unet_fa_fwd_gb300")
+    assert fa.status_string(0) == "FA_OK"
+    assert fa.status_string(4) == "FA_ERR_TIMEOUT"
+    assert fa.status_string(99) == "FA_ERR_UNKNOWN"
+
+
+FAKE = dict(q=0x10000, k=0x20000, v=0x30000, mask=None, out=0x40000, lse=0x50000,
+            B=1, H=2, Nq=100, Nk=100, D=64, scale=0.125, stream=None)
+
+
+def _call(**kw):
+    a = dict(FAKE, **kw)
+    return fa.fa_fwd_status(a["q"], a["k"], a["v"], a["mask"], a["out"], a["lse"], a["B"], a["H"],
+                            a["Nq"], a["Nk"], a["D"], a["scale"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), 1), (dict(k=None), 1), (dict(v=None), 1), (dict(out=None), 1),
+    (dict(lse=None), 1), (dict(B=0), 1), (dict(H=-1), 1), (dict(Nq=0), 1), (dict(Nk=0), 1),
+    (dict(scale=float("inf")), 1), (dict(scale=float("nan")), 1),
+    (dict(D=48), 2), (dict(D=256), 2), (dict(D=16), 2),
+    (dict(q=0x10008), 1), (dict(lse=0x50004), 1), (dict(mask=0x60004), 1),
+    (dict(out=0x10000), 1),                  # out aliases q
+    (dict(lse=0x40000 + 64), 1),             # lse inside out
+    (dict(mask=0x40000 + 32), 1),            # mask inside out
+    (dict(B=1 << 20, H=1 << 12), 1),         # B*H overflows int32
+])
+def test_validation_before_any_cuda_call(lib, kw, code):
+    assert _call(**kw) == code
+
+
+def test_valid_call_without_gpu_reports_cuda_error(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert _call() == 3
+
+
+def test_fault_injection_hook(lib, monkeypatch):
+    monkeypatch.setenv("FA_FAULT_INJECT", "launch")
+    assert _call() == 3

@@ -1,0 +1,12 @@
+"""GB300-native FlashAttention-style attention forward (sm_103a).
+
+The compute lives in a C-ABI CUDA library (``csrc/``, declared in
+``include/fa.h``); :mod:`unet_fa_fwd_gb300.binding` marshals torch tensors
+into it.  The library is loaded on first use, and every call fails loudly if
+it is missing: there is no CPU fallback.
+"""
+from .binding import (fa_fwd, fa_fwd_status, fwd, library_path, load_library,  # noqa: F401
+                      read_device_status, status_string, version)
+
+__all__ = ["fa_fwd", "fa_fwd_status", "fwd", "library_path", "load_library", "read_device_status",
+           "status_string", "version"]

@@ -1,0 +1,130 @@
+"""Python binding of the C ABI in ``include/fa.h`` (argument marshalling only).
+
+Torch provides device memory and streams; every step of the attention forward
+runs in the CUDA library.  The library is loaded on first use; if it is
+missing or cannot be loaded every call raises — there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+from . import _build
+
+FA_OK = 0
+FA_ERR_INVALID_ARGUMENT = 1
+FA_ERR_UNSUPPORTED = 2
+FA_ERR_CUDA = 3
+FA_ERR_TIMEOUT = 4
+
+_lib = None
+_lock = threading.Lock()
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load_library() -> ctypes.CDLL:
+    """Load ``libfa_fwd.so`` (built by ``__graft_entry__.build()``); raise if absent."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = library_path()
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    f"CUDA library {path} is missing: build it first (python -c 'import "
+                    "__graft_entry__ as g; g.build()'); there is no CPU fallback")
+            lib = ctypes.CDLL(path)
+            vp, i32, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+            lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp]
+            lib.fa_fwd.restype = i32
+            lib.fa_read_device_status.argtypes = [vp, ctypes.POINTER(i32)]
+            lib.fa_read_device_status.restype = i32
+            lib.fa_status_string.argtypes = [i32]
+            lib.fa_status_string.restype = ctypes.c_char_p
+            lib.fa_version.argtypes = []
+            lib.fa_version.restype = ctypes.c_char_p
+            _lib = lib
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return load_library().fa_status_string(int(code)).decode()
+
+
+def version() -> str:
+    return load_library().fa_version().decode()
+
+
+def _stream_handle(stream) -> int | None:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def fa_fwd_status(q_ptr: int, k_ptr: int, v_ptr: int, mask_ptr: int | None, out_ptr: int,
+                  lse_ptr: int, B: int, H: int, Nq: int, Nk: int, D: int, scale: float,
+                  stream: int | None) -> int:
+    """Raw call with integer pointers; returns the status code."""
+    return load_library().fa_fwd(q_ptr, k_ptr, v_ptr, mask_ptr, out_ptr, lse_ptr, B, H, Nq, Nk, D,
+                                 ctypes.c_float(scale), stream)
+
+
+def _check(t: torch.Tensor, name: str, dtype: torch.dtype, shape: tuple) -> None:
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def fa_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, mask: torch.Tensor | None,
+           out: torch.Tensor, lse: torch.Tensor, scale: float | None = None, stream=None) -> None:
+    """Enqueue the forward into caller-provided ``out`` (bf16 [B,H,Nq,D]) and ``lse`` (fp32 [B,H,Nq])."""
+    if q.dim() != 4 or k.dim() != 4:
+        raise ValueError("q, k, v must be [B, H, N, D]")
+    B, H, Nq, D = q.shape
+    Nk = k.shape[2]
+    _check(q, "q", torch.bfloat16, (B, H, Nq, D))
+    _check(k, "k", torch.bfloat16, (B, H, Nk, D))
+    _check(v, "v", torch.bfloat16, (B, H, Nk, D))
+    _check(out, "out", torch.bfloat16, (B, H, Nq, D))
+    _check(lse, "lse", torch.float32, (B, H, Nq))
+    if mask is not None:
+        _check(mask, "mask", torch.float32, (B, Nk))
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    rc = fa_fwd_status(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                       None if mask is None else mask.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                       B, H, Nq, Nk, D, float(scale), _stream_handle(stream))
+    if rc != FA_OK:
+        raise RuntimeError(f"fa_fwd failed: {status_string(rc)}")
+
+
+def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, mask: torch.Tensor | None = None,
+        scale: float | None = None, stream=None):
+    """Allocate outputs and run the forward; returns (O bf16 [B,H,Nq,D], LSE fp32 [B,H,Nq])."""
+    B, H, Nq, D = q.shape
+    out = torch.empty((B, H, Nq, D), dtype=torch.bfloat16, device=q.device)
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    fa_fwd(q, k, v, mask, out, lse, scale=scale, stream=stream)
+    return out, lse
+
+
+def read_device_status(stream=None) -> int:
+    """Synchronise and return (then reset) the device status word: FA_OK or FA_ERR_TIMEOUT."""
+    st = ctypes.c_int(0)
+    rc = load_library().fa_read_device_status(_stream_handle(stream), ctypes.byref(st))
+    if rc != FA_OK:
+        raise RuntimeError(f"fa_read_device_status failed: {status_string(rc)}")
+    return st.value

@@ -1,0 +1,213 @@
+// fa_fwd.cu — C ABI of the attention forward (declared in include/fa.h):
+// argument validation, TMA descriptor encoding and the kernel launch.
+//
+// The library is linked against the static CUDA runtime and reaches the
+// driver's tensor-map encoder through cudaGetDriverEntryPointByVersion, so it
+// loads on a machine without a GPU driver; every compute entry point then
+// fails with FA_ERR_CUDA instead of crashing.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "fa.h"
+#include "fa_fwd_kernel.cuh"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  bool ready = false;
+  bool supported = false;
+  int sm_count = 0;
+  bool attr_set[3] = {false, false, false};  // D = 32, 64, 128
+};
+
+std::mutex g_mutex;
+DeviceState g_devices[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+bool ranges_overlap(const void* a, size_t abytes, const void* b, size_t bbytes) {
+  if (!a || !b || abytes == 0 || bbytes == 0) return false;
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return a0 < b0 + bbytes && b0 < a0 + abytes;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+unsigned long long timeout_ns_from_env() {
+  const char* e = std::getenv("FA_WAIT_TIMEOUT_MS");
+  if (e && *e) {
+    char* end = nullptr;
+    unsigned long long ms = std::strtoull(e, &end, 10);
+    if (end != e && ms > 0) return ms * 1000000ull;
+  }
+  return 2000ull * 1000000ull;  // 2 s per wait; a healthy wait lasts microseconds
+}
+
+// Set-up per device: capability check, SM count, driver entry point.
+int device_setup(int dev, DeviceState** out) {
+  if (dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState& st = g_devices[dev];
+  if (!st.ready) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      return FA_ERR_CUDA;
+    }
+    st.supported = (major == 10 && minor == 3);
+    st.sm_count = sms;
+    if (!g_encode) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                           &q) != cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || fn == nullptr) {
+        return FA_ERR_CUDA;
+      }
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    st.ready = true;
+  }
+  *out = &st;
+  return FA_OK;
+}
+
+// 3-D tensor map over a contiguous bf16 [BH][N][D] tensor; box = one chunk of
+// 128 rows (inner extent = the swizzle span), swizzled to match the UMMA
+// shared-memory layout.
+int encode_map(CUtensorMap* map, const void* base, int BH, int N, int D) {
+  const int sw_bytes = (D >= 64) ? 128 : 64;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)N, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)N * D * 2};
+  cuuint32_t box[3] = {(cuuint32_t)(sw_bytes / 2), 128u, 1u};
+  cuuint32_t estride[3] = {1u, 1u, 1u};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                        strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        sw_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
+template <int D>
+int launch(const fa::Params& prm, DeviceState& st, int slot, cudaStream_t stream) {
+  using C = fa::Cfg<D>;
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!st.attr_set[slot]) {
+      if (cudaFuncSetAttribute(fa::fa_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               C::SMEM_BYTES) != cudaSuccess)
+        return FA_ERR_CUDA;
+      st.attr_set[slot] = true;
+    }
+  }
+  const int grid = prm.num_units < st.sm_count ? prm.num_units : st.sm_count;
+  fa::fa_fwd_kernel<D><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(prm);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_fwd(const void* q, const void* k, const void* v, const float* mask, void* out, float* lse,
+           int B, int H, int Nq, int Nk, int D, float scale, void* stream) {
+  // ---- validation: no CUDA call before this block passes ----
+  if (!q || !k || !v || !out || !lse) return FA_ERR_INVALID_ARGUMENT;
+  if (B < 1 || H < 1 || Nq < 1 || Nk < 1) return FA_ERR_INVALID_ARGUMENT;
+  if (!std::isfinite(scale)) return FA_ERR_INVALID_ARGUMENT;
+  if (D != 32 && D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse) ||
+      (mask && !aligned16(mask)))
+    return FA_ERR_INVALID_ARGUMENT;
+  const int64_t BH = (int64_t)B * H;
+  const int64_t qtiles = ((int64_t)Nq + 127) / 128;
+  const int64_t upb = (qtiles + 1) / 2;
+  if (BH > INT_MAX || BH * upb > INT_MAX || BH > (int64_t)UINT32_MAX) return FA_ERR_INVALID_ARGUMENT;
+  const size_t q_bytes = (size_t)BH * Nq * D * 2, kv_bytes = (size_t)BH * Nk * D * 2;
+  const size_t lse_bytes = (size_t)BH * Nq * 4, mask_bytes = mask ? (size_t)B * Nk * 4 : 0;
+  if (ranges_overlap(out, q_bytes, q, q_bytes) || ranges_overlap(out, q_bytes, k, kv_bytes) ||
+      ranges_overlap(out, q_bytes, v, kv_bytes) || ranges_overlap(out, q_bytes, lse, lse_bytes) ||
+      ranges_overlap(out, q_bytes, mask, mask_bytes) ||
+      ranges_overlap(lse, lse_bytes, q, q_bytes) || ranges_overlap(lse, lse_bytes, k, kv_bytes) ||
+      ranges_overlap(lse, lse_bytes, v, kv_bytes) ||
+      ranges_overlap(lse, lse_bytes, mask, mask_bytes))
+    return FA_ERR_INVALID_ARGUMENT;
+
+  // ---- set-up ----
+  if (std::getenv("FA_FAULT_INJECT") && std::strcmp(std::getenv("FA_FAULT_INJECT"), "launch") == 0)
+    return FA_ERR_CUDA;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  DeviceState* st = nullptr;
+  int rc = device_setup(dev, &st);
+  if (rc != FA_OK) return rc;
+  if (!st->supported) return FA_ERR_UNSUPPORTED;
+
+  fa::Params prm;
+  std::memset(&prm, 0, sizeof(prm));
+  if (encode_map(&prm.tm_q, q, (int)BH, Nq, D) != FA_OK ||
+      encode_map(&prm.tm_k, k, (int)BH, Nk, D) != FA_OK ||
+      encode_map(&prm.tm_v, v, (int)BH, Nk, D) != FA_OK)
+    return FA_ERR_CUDA;
+  prm.out = reinterpret_cast<__nv_bfloat16*>(out);
+  prm.lse = lse;
+  prm.mask = mask;
+  prm.H = H;
+  prm.Nq = Nq;
+  prm.Nk = Nk;
+  prm.units_per_bh = (int)upb;
+  prm.num_units = (int)(BH * upb);
+  prm.nkv = (Nk + 127) / 128;
+  prm.scale_log2 = (float)((double)scale * 1.4426950408889634);
+  prm.timeout_ns = timeout_ns_from_env();
+
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  switch (D) {
+    case 32: return launch<32>(prm, *st, 0, s);
+    case 64: return launch<64>(prm, *st, 1, s);
+    default: return launch<128>(prm, *st, 2, s);
+  }
+}
+
+int fa_read_device_status(void* stream, int* status) {
+  if (!status) return FA_ERR_INVALID_ARGUMENT;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int value = 0;
+  if (cudaMemcpyFromSymbolAsync(&value, fa::g_device_status, sizeof(int), 0,
+                                cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return FA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return FA_ERR_CUDA;
+  const int zero = 0;
+  if (cudaMemcpyToSymbolAsync(fa::g_device_status, &zero, sizeof(int), 0, cudaMemcpyHostToDevice,
+                              s) != cudaSuccess)
+    return FA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return FA_ERR_CUDA;
+  *status = value;
+  return FA_OK;
+}
+
+const char* fa_status_string(int status) {
+  switch (status) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_INVALID_ARGUMENT: return "FA_ERR_INVALID_ARGUMENT";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED";
+    case FA_ERR_CUDA: return "FA_ERR_CUDA";
+    case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT";
+    default: return "FA_ERR_UNKNOWN";
+  }
+}
+
+const char* fa_version(void) { return "unet_fa_fwd_gb300 0.1.0 sm_103a"; }
+
+}  // extern "C"

@@ -1,0 +1,516 @@
+// fa_fwd_kernel.cuh — the sm_103a attention-forward kernel.
+//
+// Computes, per (batch b, head h, query row i):
+//   t_ij = log2(e) * (scale * q_i . k_j + mask[b, j])       (log2-domain scores)
+//   O_i  = sum_j 2^(t_ij - m_i) v_j / sum_j 2^(t_ij - m_i),  LSE_i = ln2 * (m_i + log2 l_i)
+// FlashAttention-style: the key axis is walked in 128-key blocks with a
+// running row max m, running denominator l and a rescaled accumulator O
+// ("算子加速：注意力、编译与融合", section "注意力：从O(N²)显存到分块": the figure and
+// the `blocked` example's m / l / acc recurrence), so the score matrix never
+// leaves the SM.  exp is taken as exp2 with log2(e) folded into the scale.
+//
+// One persistent CTA per SM walks work units (b·h, 256 query rows = two
+// 128-row query tiles).  Warp roles (384 threads):
+//   warps 0-3  softmax warpgroup for query tile 0 (one thread per row)
+//   warps 4-7  softmax warpgroup for query tile 1
+//   warp  8    TMA producer: Q tiles, then K_j, V_j into a shared-memory ring
+//   warp  9    MMA issuer (one thread) and TMEM owner
+//   warps 10-11 idle
+// Tensor memory (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+D),
+// O1 [256+D, 256+2D).  P (bf16) is written over the first 64 columns of its
+// S block and fed to the P·V MMA straight from tensor memory.
+//
+// Every mbarrier wait is bounded in time: past the limit the CTA records
+// FA_ERR_TIMEOUT in a device status word, drains its own in-flight copies and
+// MMAs, frees tensor memory and returns.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "sm100_ptx.cuh"
+
+namespace fa {
+
+constexpr int kStatusTimeout = 4;  // == FA_ERR_TIMEOUT
+
+// Device status word (one per device per loaded library): 0 or a status code.
+__device__ int g_device_status = 0;
+
+template <int D>
+struct Cfg {
+  static_assert(D == 32 || D == 64 || D == 128, "head dim");
+  static constexpr int BM = 128;                       // query rows per tile
+  static constexpr int BN = 128;                       // keys per tile
+  static constexpr int SW = (D >= 64) ? 128 : 64;      // swizzle span = bytes per chunk row
+  static constexpr int CHUNK_ELEMS = SW / 2;           // bf16 per chunk row
+  static constexpr int NCHUNK = D / CHUNK_ELEMS;       // chunks across the head dim
+  static constexpr int CHUNK_BYTES = BN * SW;          // one 128-row chunk
+  static constexpr int TILE_BYTES = BN * D * 2;        // one 128-row tile (Q, K or V)
+  static constexpr int STAGES = (D == 128) ? 4 : (D == 64 ? 6 : 8);
+  static constexpr int SMEM_Q = 2 * TILE_BYTES;
+  static constexpr int SMEM_RING = STAGES * TILE_BYTES;
+  static constexpr int SMEM_BAR = 1024;
+  static constexpr int SMEM_USED = 1024 /*align slack*/ + SMEM_Q + SMEM_RING + SMEM_BAR;
+  // 512 TMEM columns per CTA => one CTA per SM; pad shared memory so that a
+  // second CTA never lands on the SM and blocks in tcgen05.alloc.
+  static constexpr int SMEM_BYTES = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;
+  static constexpr int SBO = 8 * SW;                   // bytes between 8-row core-matrix groups
+  static constexpr uint32_t LAYOUT = (SW == 128) ? 2u : 4u;  // UMMA SWIZZLE_128B / SWIZZLE_64B
+  static constexpr int TMEM_COLS = 512;
+  static constexpr int COL_S0 = 0, COL_S1 = 128, COL_O0 = 256, COL_O1 = 256 + D;
+  static constexpr int THREADS = 384;
+};
+
+struct Params {  // 64-byte aligned through its CUtensorMap members
+  CUtensorMap tm_q;  // [BH][Nq][D] bf16
+  CUtensorMap tm_k;  // [BH][Nk][D]
+  CUtensorMap tm_v;  // [BH][Nk][D]
+  __nv_bfloat16* out;  // [BH][Nq][D]
+  float* lse;          // [BH][Nq]
+  const float* mask;   // [B][Nk] or nullptr
+  int H, Nq, Nk;
+  int num_units;       // BH * units_per_bh
+  int units_per_bh;    // ceil(ceil(Nq/128)/2)
+  int nkv;             // ceil(Nk/128)
+  float scale_log2;    // scale * log2(e)
+  unsigned long long timeout_ns;
+};
+
+// Shared-memory matrix descriptor (tcgen05 "matrix descriptor"): start
+// address, leading / stride byte offsets (16-byte units), version 1,
+// swizzle layout in bits 61-63.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo,
+                                              uint32_t layout) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)layout << 61;
+  return d;
+}
+
+// Instruction descriptor for kind::f16 with bf16 A/B and fp32 accumulate.
+__host__ __device__ constexpr uint32_t make_idesc(int M, int N, bool b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+struct Barriers {
+  uint64_t q_full, q_empty;
+  uint64_t s_full[2], p_ready[2], o_full[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  volatile int abort_flag;
+  uint64_t kv_full[8], kv_empty[8];
+};
+
+// Bounded wait on an mbarrier phase.  Returns false if the CTA is aborting
+// (this wait ran out of time, or another one did).
+__device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity, Barriers* bars,
+                                             unsigned long long timeout_ns) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  uint64_t t0 = ptx::global_timer_ns();
+  uint32_t spins = 0;
+  while (true) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if ((++spins & 63u) == 0) {
+      if (bars->abort_flag) return false;
+      if (ptx::global_timer_ns() - t0 > timeout_ns) {
+        bars->abort_flag = 1;
+        atomicCAS(&g_device_status, 0, kStatusTimeout);
+        return false;
+      }
+    }
+  }
+}
+
+// Warp-uniform version: every lane waits, then the warp agrees.
+__device__ __forceinline__ bool bounded_wait_warp(uint32_t bar, uint32_t parity, Barriers* bars,
+                                                  unsigned long long timeout_ns) {
+  bool ok = bounded_wait(bar, parity, bars, timeout_ns);
+  return __all_sync(0xffffffffu, ok);
+}
+
+template <int D>
+__global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
+    fa_fwd_kernel(const __grid_constant__ Params p) {
+  using C = Cfg<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* sQ = smem;                      // 2 tiles
+  uint8_t* sRing = smem + C::SMEM_Q;       // STAGES tiles
+  Barriers* bars = reinterpret_cast<Barriers*>(sRing + C::SMEM_RING);
+
+  const int warp = threadIdx.x / 32;
+  const uint32_t lane = threadIdx.x % 32;
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(ptx::smem_u32(&bars->q_full), 1);
+    ptx::mbar_init(ptx::smem_u32(&bars->q_empty), 1);
+    for (int t = 0; t < 2; ++t) {
+      ptx::mbar_init(ptx::smem_u32(&bars->s_full[t]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bars->p_ready[t]), 128);
+      ptx::mbar_init(ptx::smem_u32(&bars->o_full[t]), 1);
+    }
+    ptx::mbar_init(ptx::smem_u32(&bars->drain), 1);
+    for (int s = 0; s < C::STAGES; ++s) {
+      ptx::mbar_init(ptx::smem_u32(&bars->kv_full[s]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bars->kv_empty[s]), 1);
+    }
+    bars->abort_flag = 0;
+    ptx::fence_barrier_init();
+  }
+  if (warp == 9) {
+    ptx::tmem_alloc(ptx::smem_u32(&bars->tmem_base), C::TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before_sync();
+  __syncthreads();
+  ptx::tc_fence_after_sync();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer --
+    if (lane == 0) {
+      ptx::tma_prefetch_desc(&p.tm_q);
+      ptx::tma_prefetch_desc(&p.tm_k);
+      ptx::tma_prefetch_desc(&p.tm_v);
+      uint32_t it = 0, uc = 0;
+      uint32_t issued[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+      uint32_t q_issued = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uc) {
+        const int bh = u / p.units_per_bh;
+        const int q0 = (u % p.units_per_bh) * 256;
+        const int ntiles = (q0 + 128 < p.Nq) ? 2 : 1;
+        ok = bounded_wait(ptx::smem_u32(&bars->q_empty), (uc & 1) ^ 1, bars, p.timeout_ns);
+        if (!ok) break;
+        const uint32_t qbar = ptx::smem_u32(&bars->q_full);
+        ptx::mbar_arrive_expect_tx(qbar, ntiles * C::TILE_BYTES);
+        for (int t = 0; t < ntiles; ++t)
+          for (int c = 0; c < C::NCHUNK; ++c)
+            ptx::tma_load_3d(ptx::smem_u32(sQ + t * C::TILE_BYTES + c * C::CHUNK_BYTES), &p.tm_q,
+                             qbar, c * C::CHUNK_ELEMS, q0 + t * 128, bh);
+        ++q_issued;
+        for (int j = 0; j < p.nkv && ok; ++j) {
+          for (int kv = 0; kv < 2; ++kv, ++it) {
+            const uint32_t s = it % C::STAGES;
+            const uint32_t ph = (it / C::STAGES) & 1;
+            ok = bounded_wait(ptx::smem_u32(&bars->kv_empty[s]), ph ^ 1, bars, p.timeout_ns);
+            if (!ok) break;
+            const uint32_t fb = ptx::smem_u32(&bars->kv_full[s]);
+            ptx::mbar_arrive_expect_tx(fb, C::TILE_BYTES);
+            const void* tm = kv == 0 ? (const void*)&p.tm_k : (const void*)&p.tm_v;
+            for (int c = 0; c < C::NCHUNK; ++c)
+              ptx::tma_load_3d(ptx::smem_u32(sRing + s * C::TILE_BYTES + c * C::CHUNK_BYTES), tm,
+                               fb, c * C::CHUNK_ELEMS, j * 128, bh);
+            ++issued[s];
+          }
+        }
+      }
+      if (!ok) {
+        // Drain: wait (bounded) until every copy this thread issued has landed.
+        const unsigned long long t_drain = p.timeout_ns;
+        for (int s = 0; s < C::STAGES; ++s) {
+          if (issued[s] == 0) continue;
+          const uint32_t bar = ptx::smem_u32(&bars->kv_full[s]);
+          uint64_t t0 = ptx::global_timer_ns();
+          while (!ptx::mbar_try_wait(bar, (issued[s] - 1) & 1) &&
+                 ptx::global_timer_ns() - t0 < t_drain) {
+          }
+        }
+        if (q_issued) {
+          const uint32_t bar = ptx::smem_u32(&bars->q_full);
+          uint64_t t0 = ptx::global_timer_ns();
+          while (!ptx::mbar_try_wait(bar, (q_issued - 1) & 1) &&
+                 ptx::global_timer_ns() - t0 < t_drain) {
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 9) {
+    // ----------------------------------------------------------------- MMA --
+    if (lane == 0) {
+      constexpr uint32_t IDESC_QK = make_idesc(128, 128, false);
+      constexpr uint32_t IDESC_PV = make_idesc(128, D, true);
+      const uint32_t sq = ptx::smem_u32(sQ);
+      const uint32_t sring = ptx::smem_u32(sRing);
+      uint32_t it = 0, uc = 0, pc0 = 0, pc1 = 0;
+      bool ok = true;
+
+      // S_t = Q_t K^T : A = Q tile (K-major), B = K tile (K-major), K-dim = D.
+      auto issue_s = [&](int t, uint32_t stage) {
+        const uint32_t a_base = sq + t * C::TILE_BYTES;
+        const uint32_t b_base = sring + stage * C::TILE_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk * 16 / C::CHUNK_ELEMS) * C::CHUNK_BYTES +
+                               (kk * 16 % C::CHUNK_ELEMS) * 2;
+          ptx::mma_ss(tmem + (t ? C::COL_S1 : C::COL_S0),
+                      smem_desc(a_base + off, 16, C::SBO, C::LAYOUT),
+                      smem_desc(b_base + off, 16, C::SBO, C::LAYOUT), IDESC_QK, kk > 0);
+        }
+      };
+      // O_t += P_t V : A = P (tensor memory, over the S_t block), B = V tile
+      // (MN-major: the head dim is contiguous), K-dim = 128 keys.
+      auto issue_pv = [&](int t, uint32_t stage, bool first) {
+        const uint32_t b_base = sring + stage * C::TILE_BYTES;
+        const uint32_t a_tmem = tmem + (t ? C::COL_S1 : C::COL_S0);
+#pragma unroll
+        for (int kk = 0; kk < 128 / 16; ++kk) {
+          ptx::mma_ts(tmem + (t ? C::COL_O1 : C::COL_O0), a_tmem + kk * 8,
+                      smem_desc(b_base + kk * 16 * C::SW, C::CHUNK_BYTES, C::SBO, C::LAYOUT),
+                      IDESC_PV, (!first || kk > 0) ? 1u : 0u);
+        }
+      };
+
+      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uc) {
+        const int q0 = (u % p.units_per_bh) * 256;
+        const bool has1 = q0 + 128 < p.Nq;
+        const int nkv = p.nkv;
+        ok = bounded_wait(ptx::smem_u32(&bars->q_full), uc & 1, bars, p.timeout_ns);
+        if (!ok) break;
+        ptx::tc_fence_after_sync();
+        // Prologue: S for key block 0.
+        uint32_t sK = it % C::STAGES;
+        ok = bounded_wait(ptx::smem_u32(&bars->kv_full[sK]), (it / C::STAGES) & 1, bars,
+                          p.timeout_ns);
+        if (!ok) break;
+        ptx::tc_fence_after_sync();
+        issue_s(0, sK);
+        ptx::mma_commit(ptx::smem_u32(&bars->s_full[0]));
+        if (has1) {
+          issue_s(1, sK);
+          ptx::mma_commit(ptx::smem_u32(&bars->s_full[1]));
+        }
+        ptx::mma_commit(ptx::smem_u32(&bars->kv_empty[sK]));
+        ++it;
+        if (nkv == 1) ptx::mma_commit(ptx::smem_u32(&bars->q_empty));
+
+        for (int j = 0; j < nkv && ok; ++j) {
+          const uint32_t sV = it % C::STAGES;
+          ok = bounded_wait(ptx::smem_u32(&bars->kv_full[sV]), (it / C::STAGES) & 1, bars,
+                            p.timeout_ns);
+          if (!ok) break;
+          ++it;
+          const bool has_next = j + 1 < nkv;
+          // O0 += P0 V_j
+          ok = bounded_wait(ptx::smem_u32(&bars->p_ready[0]), pc0 & 1, bars, p.timeout_ns);
+          if (!ok) break;
+          ++pc0;
+          ptx::tc_fence_after_sync();
+          issue_pv(0, sV, j == 0);
+          if (!has_next) ptx::mma_commit(ptx::smem_u32(&bars->o_full[0]));
+          // S0 for key block j+1 as soon as P0 has been consumed.
+          if (has_next) {
+            sK = it % C::STAGES;
+            ok = bounded_wait(ptx::smem_u32(&bars->kv_full[sK]), (it / C::STAGES) & 1, bars,
+                              p.timeout_ns);
+            if (!ok) break;
+            ptx::tc_fence_after_sync();
+            issue_s(0, sK);
+            ptx::mma_commit(ptx::smem_u32(&bars->s_full[0]));
+          }
+          if (has1) {
+            ok = bounded_wait(ptx::smem_u32(&bars->p_ready[1]), pc1 & 1, bars, p.timeout_ns);
+            if (!ok) break;
+            ++pc1;
+            ptx::tc_fence_after_sync();
+            issue_pv(1, sV, j == 0);
+            if (!has_next) ptx::mma_commit(ptx::smem_u32(&bars->o_full[1]));
+          }
+          ptx::mma_commit(ptx::smem_u32(&bars->kv_empty[sV]));
+          if (has_next) {
+            if (has1) {
+              issue_s(1, sK);
+              ptx::mma_commit(ptx::smem_u32(&bars->s_full[1]));
+            }
+            ptx::mma_commit(ptx::smem_u32(&bars->kv_empty[sK]));
+            ++it;
+            if (j + 2 == nkv) ptx::mma_commit(ptx::smem_u32(&bars->q_empty));
+          }
+        }
+      }
+      // Drain this thread's MMAs before tensor memory can be freed.
+      ptx::mma_commit(ptx::smem_u32(&bars->drain));
+      {
+        const uint32_t bar = ptx::smem_u32(&bars->drain);
+        uint64_t t0 = ptx::global_timer_ns();
+        while (!ptx::mbar_try_wait(bar, 0) && ptx::global_timer_ns() - t0 < p.timeout_ns) {
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp < 8) {
+    // ------------------------------------------------------------- softmax --
+    const int t = warp / 4;                       // query tile of this warpgroup
+    const int row = (warp % 4) * 32 + lane;       // row within the tile == TMEM lane
+    const uint32_t lane_base = (uint32_t)((warp % 4) * 32) << 16;
+    const uint32_t tS = tmem + lane_base + (t ? C::COL_S1 : C::COL_S0);
+    const uint32_t tO = tmem + lane_base + (t ? C::COL_O1 : C::COL_O0);
+    const uint32_t bar_s = ptx::smem_u32(&bars->s_full[t]);
+    const uint32_t bar_p = ptx::smem_u32(&bars->p_ready[t]);
+    const uint32_t bar_o = ptx::smem_u32(&bars->o_full[t]);
+    const float scale_log2 = p.scale_log2;
+    constexpr float kLog2e = 1.4426950408889634f;
+    constexpr float kRescaleThreshold = 8.0f;  // log2 units: P stays <= 2^8
+    uint32_t sc = 0, oc = 0;
+    bool ok = true;
+
+    for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+      const int bh = u / p.units_per_bh;
+      const int q0 = (u % p.units_per_bh) * 256;
+      if (t == 1 && !(q0 + 128 < p.Nq)) continue;
+      const int qrow = q0 + t * 128 + row;
+      const float* mask_b = p.mask ? p.mask + (size_t)(bh / p.H) * p.Nk : nullptr;
+      float m = -INFINITY;  // running max of t_ij (log2 domain)
+      float l = 0.f;        // running denominator relative to m
+
+      for (int j = 0; j < p.nkv; ++j) {
+        ok = bounded_wait_warp(bar_s, sc & 1, bars, p.timeout_ns);
+        if (!ok) break;
+        ++sc;
+        ptx::tc_fence_after_sync();
+        float s[128];
+        {
+          uint32_t r[128];
+          ptx::tmem_ld32x32b_x128(tS, r);
+#pragma unroll
+          for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(r[c]);
+        }
+        const int kbase = j * 128;
+        const bool general = (mask_b != nullptr) || (kbase + 128 > p.Nk);
+        float mx;
+        if (!general) {
+          float a0 = s[0], a1 = s[1], a2 = s[2], a3 = s[3];
+          if (scale_log2 >= 0.f) {
+#pragma unroll
+            for (int c = 4; c < 128; c += 4) {
+              a0 = fmaxf(a0, s[c]);
+              a1 = fmaxf(a1, s[c + 1]);
+              a2 = fmaxf(a2, s[c + 2]);
+              a3 = fmaxf(a3, s[c + 3]);
+            }
+            mx = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)) * scale_log2;
+          } else {
+#pragma unroll
+            for (int c = 4; c < 128; c += 4) {
+              a0 = fminf(a0, s[c]);
+              a1 = fminf(a1, s[c + 1]);
+              a2 = fminf(a2, s[c + 2]);
+              a3 = fminf(a3, s[c + 3]);
+            }
+            mx = fminf(fminf(a0, a1), fminf(a2, a3)) * scale_log2;
+          }
+        } else {
+          // Explicit log2-domain scores: scale, additive mask, -inf past Nk.
+          mx = -INFINITY;
+#pragma unroll
+          for (int c = 0; c < 128; ++c) {
+            const int key = kbase + c;
+            float tv = -INFINITY;
+            if (key < p.Nk) {
+              tv = s[c] * scale_log2;
+              if (mask_b) tv = fmaf(__ldg(mask_b + key), kLog2e, tv);
+            }
+            s[c] = tv;
+            mx = fmaxf(mx, tv);
+          }
+        }
+        const float m_new = fmaxf(m, mx);
+        // Rescale only when the max grew by more than the threshold (or on the
+        // first finite max); otherwise keep the stale max, which is exact
+        // because the final O / l uses the same max.
+        const bool grow = (m_new - m) > kRescaleThreshold;  // -inf - -inf = NaN -> false
+        float alpha = 1.f;
+        if (grow) {
+          alpha = ptx::ex2(m - m_new);  // m = -inf -> 0
+          m = m_new;
+        }
+        const float m_use = (m == -INFINITY) ? 0.f : m;
+        l *= alpha;
+        float lsum0 = 0.f, lsum1 = 0.f;
+#pragma unroll
+        for (int cb = 0; cb < 128; cb += 32) {
+          uint32_t packed[16];
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            float p0, p1;
+            if (!general) {
+              p0 = ptx::ex2(fmaf(s[cb + c], scale_log2, -m_use));
+              p1 = ptx::ex2(fmaf(s[cb + c + 1], scale_log2, -m_use));
+            } else {
+              p0 = ptx::ex2(s[cb + c] - m_use);
+              p1 = ptx::ex2(s[cb + c + 1] - m_use);
+            }
+            lsum0 += p0;
+            lsum1 += p1;
+            packed[c / 2] = ptx::pack_bf16x2(p0, p1);
+          }
+          ptx::tmem_st32x32b_x16(tS + cb / 2, packed);
+        }
+        l += lsum0 + lsum1;
+        // Rescale the accumulator O (after P(j-1)·V has landed: the S commit
+        // that released this iteration follows that MMA).
+        if (j > 0 && __any_sync(0xffffffffu, grow)) {
+#pragma unroll
+          for (int cb = 0; cb < D; cb += 32) {
+            uint32_t r[32];
+            ptx::tmem_ld32x32b_x32(tO + cb, r);
+#pragma unroll
+            for (int c = 0; c < 32; ++c) r[c] = __float_as_uint(__uint_as_float(r[c]) * alpha);
+            ptx::tmem_st32x32b_x32(tO + cb, r);
+          }
+        }
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before_sync();
+        ptx::mbar_arrive(bar_p);
+      }
+      if (!ok) break;
+
+      // Epilogue: O / l -> bf16, LSE = ln2 * (m + log2 l).
+      ok = bounded_wait_warp(bar_o, oc & 1, bars, p.timeout_ns);
+      if (!ok) break;
+      ++oc;
+      ptx::tc_fence_after_sync();
+      const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+      const bool valid_row = qrow < p.Nq;
+      __nv_bfloat16* orow = p.out + ((size_t)bh * p.Nq + (valid_row ? qrow : 0)) * D;
+#pragma unroll
+      for (int cb = 0; cb < D; cb += 32) {
+        uint32_t r[32];
+        ptx::tmem_ld32x32b_x32(tO + cb, r);
+        uint32_t packed[16];
+#pragma unroll
+        for (int c = 0; c < 32; c += 2)
+          packed[c / 2] = ptx::pack_bf16x2(__uint_as_float(r[c]) * inv_l,
+                                           __uint_as_float(r[c + 1]) * inv_l);
+        if (valid_row) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + cb);
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4)
+            dst[v4] = make_uint4(packed[4 * v4], packed[4 * v4 + 1], packed[4 * v4 + 2],
+                                 packed[4 * v4 + 3]);
+        }
+      }
+      if (valid_row) {
+        constexpr float kLn2 = 0.6931471805599453f;
+        p.lse[(size_t)bh * p.Nq + qrow] = (l > 0.f) ? (m + __log2f(l)) * kLn2 : -INFINITY;
+      }
+    }
+    ptx::tc_fence_before_sync();
+  }
+
+  __syncthreads();
+  if (warp == 9) {
+    ptx::tc_fence_after_sync();
+    ptx::tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+}  // namespace fa
