@@ -1,0 +1,422 @@
+#!/usr/bin/env python3
+"""Benchmark of the attention forward: attention TFLOP/s on one GB300, next to
+the fp64 CPU oracle.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl native|reference]
+
+A step is one attention forward (one kernel launch) over the whole workload,
+inputs resident in device memory.  Default workload: FLUX 2048² joint
+attention, B1 H24 N16896 D128 bf16 (Q/K/V 311 MB, larger than the 129 MB L2,
+so no flush is needed between steps).  Prints one JSON line on rank 0.
+
+N > 1 (under torchrun) runs one independent replica per GPU — the path has no
+exchange step — and reports the whole-job throughput (weak scaling).
+``--impl reference`` times the CPU oracle instead, on a bounded sample of the
+same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd TFLOP/s and % of GB300 dense-bf16 peak (1 GPU), vs CPU oracle"
+FALLBACK_BF16_TFLOPS = 1900.0
+KERNEL_NAME = "fa_fwd_kernel"
+
+
+# --------------------------------------------------------------------- helpers
+
+def kernel_source_hash() -> str:
+    """sha256 over the CUDA sources and the C header (identifies a kernel build)."""
+    from unet_fa_fwd_gb300 import _build
+    h = hashlib.sha256()
+    for path in _build.sources():
+        with open(path, "rb") as f:
+            h.update(os.path.basename(path).encode())
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            peaks = json.load(f)
+        return peaks, "measured"
+    except (OSError, ValueError):
+        return {"bf16_tflops": FALLBACK_BF16_TFLOPS}, "fallback"
+
+
+def read_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on this kernel."""
+    path = os.path.join(ROOT, "profiles", f"{KERNEL_NAME}_{workload}_traffic.txt")
+    try:
+        kv = {}
+        with open(path) as f:
+            for line in f:
+                if ":" in line and not line.startswith("#"):
+                    k, v = line.split(":", 1)
+                    kv[k.strip()] = v.strip()
+        if kv.get("kernel_source_sha256") != kernel_source_hash():
+            return None
+        return int(float(kv["dram_bytes_per_launch"]))
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.hw_slowdown",
+              "clocks_event_reasons.hw_thermal_slowdown", "clocks_event_reasons.sw_thermal_slowdown",
+              "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, device_index: int):
+        self.device_index = device_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.device_index), "--query-gpu=" + ",".join(self.FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        if not self.lines:
+            return None
+        sm, smax, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax = max(smax, float(parts[1]))
+            except ValueError:
+                continue
+            for n, p in zip(names, parts[3:7]):
+                if p.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        busy = [s for s in sm if s > 0.5 * smax] or sm
+        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- distributed
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(value: float, group=None, device=None) -> float:
+    """Max of a per-rank float over the process group (identity when not distributed)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size(group) == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX, group=group)
+    return float(t.item())
+
+
+def whole_job_throughput(units_per_rank: float, world: int, max_seconds: float) -> float:
+    """Units processed by all ranks divided by the slowest rank's time."""
+    return units_per_rank * world / max_seconds
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+class OracleSampler:
+    """The fp64 CPU oracle on seeded query rows of a workload (all keys per row)."""
+
+    def __init__(self, inp, seed: int = 12345):
+        import oracle
+        from unet_fa_fwd_gb300 import workloads
+
+        self.oracle, self.workloads = oracle, workloads
+        self.inp = inp
+        self.seed = seed
+        self.shape = inp["shape"]
+        self.mask = None if inp["mask"] is None else inp["mask"].cpu().numpy()
+        self.qkv = [workloads.to_host_bits(inp[n]) for n in "qkv"]
+        self.threads = oracle.default_threads()
+
+    def run(self, rows_per_head: int):
+        """Returns (flops, seconds, rows_per_head actually used)."""
+        B, H, Nq, Nk, D = self.shape
+        rows = self.workloads.sample_rows(Nq, B * H, rows_per_head, seed=self.seed)
+        t0 = time.perf_counter()
+        self.oracle.attention(*self.qkv, mask=self.mask, scale=self.inp["scale"], rows=rows,
+                              nthreads=self.threads)
+        dt = time.perf_counter() - t0
+        return 4.0 * B * H * rows.shape[1] * Nk * D, dt, rows.shape[1]
+
+    def rows_for(self, budget_s: float) -> int:
+        """Rows per head whose oracle time is about budget_s (calibrated on one row per head)."""
+        B, H, Nq, Nk, D = self.shape
+        _, dt, r = self.run(2)
+        per_row = dt / (r * B * H)
+        return int(max(1, min(Nq, budget_s / max(per_row, 1e-9) / (B * H))))
+
+
+# ---------------------------------------------------------------------- main
+
+def bench_native(args, world, rank, local):
+    import torch
+    import torch.distributed as dist
+
+    import unet_fa_fwd_gb300 as fa
+    from unet_fa_fwd_gb300 import accounting, workloads
+
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=device)
+    fa.load_library()
+
+    w = workloads.WORKLOADS[args.workload]
+    inp = workloads.make_inputs(w, device=device)
+    B, H, Nq, Nk, D = inp["shape"]
+    q, k, v, mask = inp["q"], inp["k"], inp["v"], inp["mask"]
+    out = torch.empty_like(q)
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=device)
+    flops = accounting.attention_flops(B, H, Nq, Nk, D)
+    in_bytes = sum(t.numel() * t.element_size() for t in (q, k, v)) + (
+        0 if mask is None else mask.numel() * 4)
+    stream = torch.cuda.current_stream(device)
+
+    def step():
+        fa.fa_fwd(q, k, v, mask, out, lse, scale=inp["scale"], stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(device)
+    if fa.read_device_status(stream) != 0:
+        raise RuntimeError("kernel wait timed out during warm-up")
+
+    # ---- device-resident timed region ----
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(device)
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        if world > 1:
+            dist.barrier()
+    secs = e0.elapsed_time(e1) / 1e3
+    max_secs = max_over_ranks(secs, device=device)
+    if fa.read_device_status(stream) != 0:
+        raise RuntimeError("kernel wait timed out in the timed region")
+    value_tflops = whole_job_throughput(flops * args.steps, world, max_secs) / 1e12
+    ms_per_step = max_secs * 1e3 / args.steps
+    kernel_tflops = flops / (ms_per_step / 1e3) / 1e12
+
+    # ---- end to end: pinned host inputs -> device -> fa_fwd -> host outputs ----
+    hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
+    hmask = None if mask is None else mask.cpu().pin_memory()
+    hout = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    hlse = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dmask = None if mask is None else torch.empty_like(mask)
+
+    def e2e_step():
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        if dmask is not None:
+            dmask.copy_(hmask, non_blocking=True)
+        fa.fa_fwd(dq, dk, dv, dmask, out, lse, scale=inp["scale"], stream=stream)
+        hout.copy_(out, non_blocking=True)
+        hlse.copy_(lse, non_blocking=True)
+
+    e2e_steps = max(3, args.steps // 20)
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(device)
+    if world > 1:
+        dist.barrier()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    torch.cuda.synchronize(device)
+    e2e_secs = max_over_ranks(time.perf_counter() - t0, device=device)
+    e2e_tflops = whole_job_throughput(flops * e2e_steps, world, e2e_secs) / 1e12
+    out_bytes = out.numel() * 2 + lse.numel() * 4
+
+    # ---- secondary workload: HunyuanVideo 720p (few steps) ----
+    also = {}
+    if args.also and rank == 0 and args.workload != "hunyuan_720p":
+        del dq, dk, dv, hq, hk, hv
+        hw = workloads.make_inputs("hunyuan_720p", device=device)
+        hB, hH, hNq, hNk, hD = hw["shape"]
+        hoAll = torch.empty_like(hw["q"])
+        hl = torch.empty((hB, hH, hNq), dtype=torch.float32, device=device)
+        for _ in range(2):
+            fa.fa_fwd(hw["q"], hw["k"], hw["v"], None, hoAll, hl, scale=hw["scale"], stream=stream)
+        torch.cuda.synchronize(device)
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n_h = 5
+        a0.record(stream)
+        for _ in range(n_h):
+            fa.fa_fwd(hw["q"], hw["k"], hw["v"], None, hoAll, hl, scale=hw["scale"], stream=stream)
+        a1.record(stream)
+        torch.cuda.synchronize(device)
+        hms = a0.elapsed_time(a1) / n_h
+        hfl = accounting.attention_flops(hB, hH, hNq, hNk, hD)
+        also["hunyuan_720p"] = {"ms_per_step": round(hms, 3), "tflops": round(hfl / hms / 1e9, 1),
+                                "steps": n_h}
+        del hw, hoAll, hl
+
+    peaks, peak_src = read_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS))
+    for v_ in also.values():
+        v_["frac_of_peak"] = round(v_["tflops"] / peak, 4)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        sampler = OracleSampler(inp)
+        cflops, csecs, rows = sampler.run(sampler.rows_for(args.cpu_budget))
+        cpu = {"value": cflops / csecs / 1e12, "unit": "TFLOP/s", "cores": sampler.threads,
+               "kind": "oracle",
+               "sample": f"{rows} seeded query rows per head x {B * H} heads of {args.workload} "
+                         f"(all {Nk} keys), fp64 C oracle, {csecs:.1f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC,
+            "value": round(value_tflops, 2),
+            "unit": "TFLOP/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": round(ms_per_step, 4),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": args.workload, "B": B, "H": H, "Nq": Nq, "Nk": Nk, "D": D,
+                       "masked": mask is not None, "parallelism": f"replicas{world}",
+                       "l2": f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB of Q/K/V per step)"},
+            "pct_of_peak": round(100.0 * kernel_tflops / peak, 2),
+            "clocks": clocks.summary(),
+            "e2e": {"value": round(e2e_tflops, 2), "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": out_bytes},
+            "gpu_launches": args.steps,
+            "roofline": {"bound": "tensor", "achieved": round(kernel_tflops, 2), "peak": peak,
+                         "unit": "TFLOP/s", "frac": round(kernel_tflops / peak, 4),
+                         "traffic": read_traffic(args.workload),
+                         "peak_source": f"{peak_src} bf16_tflops (burst; kernel timed alone)",
+                         "algorithmic_flops_per_launch": flops,
+                         "algorithmic_bytes_per_launch": accounting.algorithmic_bytes(
+                             B, H, Nq, Nk, D, masked=mask is not None)},
+            "cpu_baseline": cpu,
+        }
+        if also:
+            line["also"] = also
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def bench_reference(args, world, rank, local):
+    """The CPU oracle as it stands, on the machine's host cores, per step a bounded sample."""
+    if rank != 0:
+        return
+    from unet_fa_fwd_gb300 import workloads
+
+    w = workloads.WORKLOADS[args.workload]
+    inp = workloads.make_inputs(w, device="cpu")
+    B, H, Nq, Nk, D = inp["shape"]
+    per_step = max(0.05, min(2.0, args.ref_budget / max(1, args.steps + args.warmup)))
+    sampler = OracleSampler(inp)
+    threads = sampler.threads
+    nrows = sampler.rows_for(per_step)
+    for _ in range(args.warmup):
+        sampler.run(nrows)
+    tot_f, tot_s, rows = 0.0, 0.0, nrows
+    for _ in range(args.steps):
+        f, s, rows = sampler.run(nrows)
+        tot_f += f
+        tot_s += s
+    value = tot_f / tot_s / 1e12
+    line = {
+        "impl": "reference",
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * tot_s / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "B": B, "H": H, "Nq": Nq, "Nk": Nk, "D": D,
+                   "masked": inp["mask"] is not None, "parallelism": "cpu"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": f"per step {rows} seeded query rows per head x {B * H} heads "
+                                   f"(all {Nk} keys), fp64 C oracle"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="flux_2048")
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--ref-budget", type=float, default=90.0, help="seconds of oracle work, reference arm")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-also", dest="also", action="store_false")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_env()
+    if args.gpus != world:
+        if world == 1 and args.gpus > 1:
+            ap.error("--gpus N > 1 runs under torchrun (one process per GPU)")
+    if args.impl == "reference":
+        bench_reference(args, world, rank, local)
+    else:
+        bench_native(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()

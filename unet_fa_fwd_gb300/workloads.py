@@ -163,6 +163,8 @@ def sample_rows(Nq: int, BH: int, nrows: int = 512, seed: int = 0) -> np.ndarray
     """
     if Nq <= nrows:
         return np.tile(np.arange(Nq, dtype=np.int64), (BH, 1))
+    if nrows == 1:
+        return np.zeros((BH, 1), dtype=np.int64)
     rows = np.empty((BH, nrows), dtype=np.int64)
     for bh in range(BH):
         rng = np.random.default_rng([seed, bh])
