@@ -108,6 +108,13 @@ int launch(const fa::Params& prm, DeviceState& st, int slot, cudaStream_t stream
       if (cudaFuncSetAttribute(fa::fa_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                C::SMEM_BYTES) != cudaSuccess)
         return FA_ERR_CUDA;
+      // The warpgroup register split (setmaxnreg) must fit in the registers
+      // the launch reserves, or the increase would wait forever: refuse to
+      // launch a build where it does not.
+      cudaFuncAttributes fattr;
+      if (cudaFuncGetAttributes(&fattr, fa::fa_fwd_kernel<D>) != cudaSuccess) return FA_ERR_CUDA;
+      if (2 * 128 * C::REGS_SOFTMAX + 128 * C::REGS_OTHER > fattr.numRegs * C::THREADS)
+        return FA_ERR_UNSUPPORTED;
       st.attr_set[slot] = true;
     }
   }

@@ -61,6 +61,17 @@ struct Cfg {
   static constexpr int TMEM_COLS = 512;
   static constexpr int COL_S0 = 0, COL_S1 = 128, COL_O0 = 256, COL_O1 = 256 + D;
   static constexpr int THREADS = 384;
+  // Launch: 168 registers x 384 threads.  The softmax warpgroups (0, 1)
+  // rise to REGS_SOFTMAX, warpgroup 2 (producer, MMA, idle) drops to
+  // REGS_OTHER; the sum stays within 384*168, so the increase never waits on
+  // registers that do not exist.
+#ifndef FA_REGS_SOFTMAX
+#define FA_REGS_SOFTMAX 192
+#define FA_REGS_OTHER 120
+#endif
+  static constexpr int REGS_SOFTMAX = FA_REGS_SOFTMAX;
+  static constexpr int REGS_OTHER = FA_REGS_OTHER;
+  static_assert(2 * 128 * REGS_SOFTMAX + 128 * REGS_OTHER <= THREADS * 168, "register split");
 };
 
 struct Params {  // 64-byte aligned through its CUtensorMap members
@@ -134,6 +145,40 @@ __device__ __forceinline__ bool bounded_wait_warp(uint32_t bar, uint32_t parity,
   return __all_sync(0xffffffffu, ok);
 }
 
+// Which columns (position within a 32-column chunk, step 2) take their exp2 on
+// the FMA pipe instead of the MUFU unit: FA_EMU_PAIRS of the 16 pairs.  Off
+// by default: on GB300 every share tried (2/16 .. 8/16 pairs) was slower than
+// none, the extra issue slots costing more than the MUFU time saved.
+#ifndef FA_EMU_PAIRS
+#define FA_EMU_PAIRS 0
+#endif
+__host__ __device__ constexpr bool kEmulatedExp2(int c) { return (c / 2) % 16 < FA_EMU_PAIRS; }
+
+// 2^x for a pair of fp32 values on the FMA pipe (Cody–Waite style range
+// reduction plus a polynomial): x = n + f with n = round(x) (by adding
+// 1.5·2^23, whose low mantissa bits then hold n) and f in [-1/2, 1/2];
+// 2^f ≈ c0 + c1 f + c2 f² + c3 f³ with coefficients from a Remez (minimax
+// relative error) fit on [-1/2, 1/2] — max relative error 7.5e-5, below the
+// bf16 rounding of P (2^-9); n is added into the exponent field.  x is
+// clamped at -126 so the result stays a non-negative float (the true value
+// there is below 2^-125 and does not matter next to the row maximum 2^0).
+__device__ __forceinline__ float2 exp2_fma_pipe(float2 x) {
+  constexpr float kRound = 12582912.0f;  // 1.5 * 2^23
+  constexpr float c0 = 0.99992805719375610f, c1 = 0.69326096773147583f;
+  constexpr float c2 = 0.24261112511157990f, c3 = 0.05517166852951050f;
+  x.x = fmaxf(x.x, -126.f);
+  x.y = fmaxf(x.y, -126.f);
+  const float2 j = __fadd2_rn(x, make_float2(kRound, kRound));
+  const float2 n = __fadd2_rn(j, make_float2(-kRound, -kRound));
+  const float2 f = __ffma2_rn(n, make_float2(-1.f, -1.f), x);
+  float2 q = __ffma2_rn(f, make_float2(c3, c3), make_float2(c2, c2));
+  q = __ffma2_rn(q, f, make_float2(c1, c1));
+  q = __ffma2_rn(q, f, make_float2(c0, c0));
+  const uint32_t b0 = __float_as_uint(q.x) + (__float_as_uint(j.x) << 23);
+  const uint32_t b1 = __float_as_uint(q.y) + (__float_as_uint(j.y) << 23);
+  return make_float2(__uint_as_float(b0), __uint_as_float(b1));
+}
+
 template <int D>
 __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     fa_fwd_kernel(const __grid_constant__ Params p) {
@@ -173,6 +218,21 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
   ptx::tc_fence_after_sync();
   const uint32_t tmem = bars->tmem_base;
 
+  // Every role ends here (its own inlined copy, so code running under
+  // different register limits never merges): all warps meet, then the TMEM
+  // owner frees the columns.
+  auto finish = [&]() {
+    ptx::named_barrier_sync(1, C::THREADS);
+    if (warp == 9) {
+      ptx::tc_fence_after_sync();
+      ptx::tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+  };
+
+  if (warp >= 8) {
+  // Warpgroup 2 gives registers to the softmax warpgroups (same PC for its
+  // four warps; code under different register limits never shares a path).
+  ptx::setmaxnreg_dec<C::REGS_OTHER>();
   if (warp == 8) {
     // ------------------------------------------------------------ producer --
     if (lane == 0) {
@@ -346,7 +406,13 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       }
     }
     __syncwarp();
-  } else if (warp < 8) {
+  }
+  finish();  // warps 8-11
+  return;
+  }
+
+  ptx::setmaxnreg_inc<C::REGS_SOFTMAX>();
+  {
     // ------------------------------------------------------------- softmax --
     const int t = warp / 4;                       // query tile of this warpgroup
     const int row = (warp % 4) * 32 + lane;       // row within the tile == TMEM lane
@@ -384,31 +450,22 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
           for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(r[c]);
         }
         const int kbase = j * 128;
-        const bool general = (mask_b != nullptr) || (kbase + 128 > p.Nk);
+        // Fast path: full key block, no mask, non-negative scale — the row max
+        // is taken on raw scores and scaled once.  Otherwise scores are
+        // materialised in the log2 domain with the mask and the Nk tail.
+        const bool general = (mask_b != nullptr) || (kbase + 128 > p.Nk) || !(scale_log2 >= 0.f);
         float mx;
         if (!general) {
           float a0 = s[0], a1 = s[1], a2 = s[2], a3 = s[3];
-          if (scale_log2 >= 0.f) {
 #pragma unroll
-            for (int c = 4; c < 128; c += 4) {
-              a0 = fmaxf(a0, s[c]);
-              a1 = fmaxf(a1, s[c + 1]);
-              a2 = fmaxf(a2, s[c + 2]);
-              a3 = fmaxf(a3, s[c + 3]);
-            }
-            mx = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)) * scale_log2;
-          } else {
-#pragma unroll
-            for (int c = 4; c < 128; c += 4) {
-              a0 = fminf(a0, s[c]);
-              a1 = fminf(a1, s[c + 1]);
-              a2 = fminf(a2, s[c + 2]);
-              a3 = fminf(a3, s[c + 3]);
-            }
-            mx = fminf(fminf(a0, a1), fminf(a2, a3)) * scale_log2;
+          for (int c = 4; c < 128; c += 8) {
+            a0 = ptx::fmax3(a0, s[c], s[c + 1]);
+            a1 = ptx::fmax3(a1, s[c + 2], s[c + 3]);
+            a2 = ptx::fmax3(a2, s[c + 4], s[c + 5]);
+            a3 = ptx::fmax3(a3, s[c + 6], s[c + 7]);
           }
+          mx = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)) * scale_log2;
         } else {
-          // Explicit log2-domain scores: scale, additive mask, -inf past Nk.
           mx = -INFINITY;
 #pragma unroll
           for (int c = 0; c < 128; ++c) {
@@ -434,27 +491,43 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         }
         const float m_use = (m == -INFINITY) ? 0.f : m;
         l *= alpha;
-        float lsum0 = 0.f, lsum1 = 0.f;
+        float2 lsum = make_float2(0.f, 0.f);
+        if (!general) {
+          const float2 sc2 = make_float2(scale_log2, scale_log2);
+          const float2 nm2 = make_float2(-m_use, -m_use);
 #pragma unroll
-        for (int cb = 0; cb < 128; cb += 32) {
-          uint32_t packed[16];
+          for (int cb = 0; cb < 128; cb += 32) {
+            uint32_t packed[16];
 #pragma unroll
-          for (int c = 0; c < 32; c += 2) {
-            float p0, p1;
-            if (!general) {
-              p0 = ptx::ex2(fmaf(s[cb + c], scale_log2, -m_use));
-              p1 = ptx::ex2(fmaf(s[cb + c + 1], scale_log2, -m_use));
-            } else {
-              p0 = ptx::ex2(s[cb + c] - m_use);
-              p1 = ptx::ex2(s[cb + c + 1] - m_use);
+            for (int c = 0; c < 32; c += 2) {
+              // x <= threshold (8) by construction of the stale max.
+              const float2 x = __ffma2_rn(make_float2(s[cb + c], s[cb + c + 1]), sc2, nm2);
+              float2 pr;
+              if (kEmulatedExp2(c)) {
+                pr = exp2_fma_pipe(x);
+              } else {
+                pr = make_float2(ptx::ex2(x.x), ptx::ex2(x.y));
+              }
+              lsum = __fadd2_rn(lsum, pr);
+              packed[c / 2] = ptx::pack_bf16x2(pr.x, pr.y);
             }
-            lsum0 += p0;
-            lsum1 += p1;
-            packed[c / 2] = ptx::pack_bf16x2(p0, p1);
+            ptx::tmem_st32x32b_x16(tS + cb / 2, packed);
           }
-          ptx::tmem_st32x32b_x16(tS + cb / 2, packed);
+        } else {
+#pragma unroll
+          for (int cb = 0; cb < 128; cb += 32) {
+            uint32_t packed[16];
+#pragma unroll
+            for (int c = 0; c < 32; c += 2) {
+              const float p0 = ptx::ex2(s[cb + c] - m_use);
+              const float p1 = ptx::ex2(s[cb + c + 1] - m_use);
+              lsum = __fadd2_rn(lsum, make_float2(p0, p1));
+              packed[c / 2] = ptx::pack_bf16x2(p0, p1);
+            }
+            ptx::tmem_st32x32b_x16(tS + cb / 2, packed);
+          }
         }
-        l += lsum0 + lsum1;
+        l += lsum.x + lsum.y;
         // Rescale the accumulator O (after P(j-1)·V has landed: the S commit
         // that released this iteration follows that MMA).
         if (j > 0 && __any_sync(0xffffffffu, grow)) {
@@ -505,12 +578,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     }
     ptx::tc_fence_before_sync();
   }
-
-  __syncthreads();
-  if (warp == 9) {
-    ptx::tc_fence_after_sync();
-    ptx::tmem_dealloc(tmem, C::TMEM_COLS);
-  }
+  finish();  // softmax warps 0-7
 }
 
 }  // namespace fa
