@@ -34,6 +34,7 @@
 namespace fa {
 
 constexpr int kStatusTimeout = 4;  // == FA_ERR_TIMEOUT
+constexpr uint32_t kSuspendNs = 20000;  // longest sleep inside one mbarrier poll
 
 // Device status word (one per device per loaded library): 0 or a status code.
 __device__ int g_device_status = 0;
@@ -48,7 +49,11 @@ struct Cfg {
   static constexpr int NCHUNK = D / CHUNK_ELEMS;       // chunks across the head dim
   static constexpr int CHUNK_BYTES = BN * SW;          // one 128-row chunk
   static constexpr int TILE_BYTES = BN * D * 2;        // one 128-row tile (Q, K or V)
-  static constexpr int STAGES = (D == 128) ? 4 : (D == 64 ? 6 : 8);
+#ifndef FA_STAGES_D128
+#define FA_STAGES_D128 5
+#endif
+  // K/V ring depth: as deep as shared memory allows (227 KB per CTA).
+  static constexpr int STAGES = (D == 128) ? FA_STAGES_D128 : (D == 64 ? 6 : 8);
   static constexpr int SMEM_Q = 2 * TILE_BYTES;
   static constexpr int SMEM_RING = STAGES * TILE_BYTES;
   static constexpr int SMEM_BAR = 1024;
@@ -56,6 +61,7 @@ struct Cfg {
   // 512 TMEM columns per CTA => one CTA per SM; pad shared memory so that a
   // second CTA never lands on the SM and blocks in tcgen05.alloc.
   static constexpr int SMEM_BYTES = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;
+  static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
   static constexpr int SBO = 8 * SW;                   // bytes between 8-row core-matrix groups
   static constexpr uint32_t LAYOUT = (SW == 128) ? 2u : 4u;  // UMMA SWIZZLE_128B / SWIZZLE_64B
   static constexpr int TMEM_COLS = 512;
@@ -119,21 +125,19 @@ struct Barriers {
 };
 
 // Bounded wait on an mbarrier phase.  Returns false if the CTA is aborting
-// (this wait ran out of time, or another one did).
+// (this wait ran out of time, or another one did).  Between polls the thread
+// sleeps in try_wait (woken when the phase completes).
 __device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity, Barriers* bars,
                                              unsigned long long timeout_ns) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
-  uint64_t t0 = ptx::global_timer_ns();
-  uint32_t spins = 0;
+  const uint64_t t0 = ptx::global_timer_ns();
   while (true) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
-    if ((++spins & 63u) == 0) {
-      if (bars->abort_flag) return false;
-      if (ptx::global_timer_ns() - t0 > timeout_ns) {
-        bars->abort_flag = 1;
-        atomicCAS(&g_device_status, 0, kStatusTimeout);
-        return false;
-      }
+    if (ptx::mbar_try_wait_sleep(bar, parity, kSuspendNs)) return true;
+    if (bars->abort_flag) return false;
+    if (ptx::global_timer_ns() - t0 > timeout_ns) {
+      bars->abort_flag = 1;
+      atomicCAS(&g_device_status, 0, kStatusTimeout);
+      return false;
     }
   }
 }
@@ -300,33 +304,52 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       constexpr uint32_t IDESC_PV = make_idesc(128, D, true);
       const uint32_t sq = ptx::smem_u32(sQ);
       const uint32_t sring = ptx::smem_u32(sRing);
-      uint32_t it = 0, uc = 0, pc0 = 0, pc1 = 0;
+      uint32_t uc = 0, pc0 = 0, pc1 = 0;
+      uint32_t stage = 0, phase = 0;  // ring position as running counters (no division)
       bool ok = true;
 
+      // Shared-memory descriptors are built once; per k-step only the start
+      // address (low 14 bits, in 16-byte units) moves, which never carries
+      // out of its field because shared memory is below 256 KB.
+      constexpr uint32_t kTile16 = C::TILE_BYTES >> 4;
+      const uint64_t dq0 = smem_desc(sq, 16, C::SBO, C::LAYOUT);
+      const uint64_t dk0 = smem_desc(sring, 16, C::SBO, C::LAYOUT);
+      const uint64_t dv0 = smem_desc(sring, C::CHUNK_BYTES, C::SBO, C::LAYOUT);
+
       // S_t = Q_t K^T : A = Q tile (K-major), B = K tile (K-major), K-dim = D.
-      auto issue_s = [&](int t, uint32_t stage) {
-        const uint32_t a_base = sq + t * C::TILE_BYTES;
-        const uint32_t b_base = sring + stage * C::TILE_BYTES;
+      auto issue_s = [&](int t, uint32_t stg) {
+        const uint64_t a = dq0 + (uint64_t)(t * kTile16);
+        const uint64_t b = dk0 + (uint64_t)(stg * kTile16);
+        const uint32_t d = tmem + (t ? C::COL_S1 : C::COL_S0);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk * 16 / C::CHUNK_ELEMS) * C::CHUNK_BYTES +
-                               (kk * 16 % C::CHUNK_ELEMS) * 2;
-          ptx::mma_ss(tmem + (t ? C::COL_S1 : C::COL_S0),
-                      smem_desc(a_base + off, 16, C::SBO, C::LAYOUT),
-                      smem_desc(b_base + off, 16, C::SBO, C::LAYOUT), IDESC_QK, kk > 0);
+          constexpr int kPerChunk = C::CHUNK_ELEMS / 16;
+          const uint32_t off = ((kk / kPerChunk) * C::CHUNK_BYTES + (kk % kPerChunk) * 32) >> 4;
+          ptx::mma_ss(d, a + off, b + off, IDESC_QK, kk > 0);
         }
       };
       // O_t += P_t V : A = P (tensor memory, over the S_t block), B = V tile
       // (MN-major: the head dim is contiguous), K-dim = 128 keys.
-      auto issue_pv = [&](int t, uint32_t stage, bool first) {
-        const uint32_t b_base = sring + stage * C::TILE_BYTES;
+      auto issue_pv = [&](int t, uint32_t stg, bool first) {
+        const uint64_t b = dv0 + (uint64_t)(stg * kTile16);
         const uint32_t a_tmem = tmem + (t ? C::COL_S1 : C::COL_S0);
+        const uint32_t d = tmem + (t ? C::COL_O1 : C::COL_O0);
 #pragma unroll
         for (int kk = 0; kk < 128 / 16; ++kk) {
-          ptx::mma_ts(tmem + (t ? C::COL_O1 : C::COL_O0), a_tmem + kk * 8,
-                      smem_desc(b_base + kk * 16 * C::SW, C::CHUNK_BYTES, C::SBO, C::LAYOUT),
-                      IDESC_PV, (!first || kk > 0) ? 1u : 0u);
+          ptx::mma_ts(d, a_tmem + kk * 8, b + (uint64_t)((kk * 16 * C::SW) >> 4), IDESC_PV,
+                      (!first || kk > 0) ? 1u : 0u);
         }
+      };
+      // Wait until the ring's current stage is full; returns that stage.
+      auto take_stage = [&](uint32_t& stg) -> bool {
+        stg = stage;
+        const bool r = bounded_wait(ptx::smem_u32(&bars->kv_full[stage]), phase, bars, p.timeout_ns);
+        if (++stage == (uint32_t)C::STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+        ptx::tc_fence_after_sync();
+        return r;
       };
 
       for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uc) {
@@ -337,11 +360,9 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         if (!ok) break;
         ptx::tc_fence_after_sync();
         // Prologue: S for key block 0.
-        uint32_t sK = it % C::STAGES;
-        ok = bounded_wait(ptx::smem_u32(&bars->kv_full[sK]), (it / C::STAGES) & 1, bars,
-                          p.timeout_ns);
+        uint32_t sK = 0, sV = 0;
+        ok = take_stage(sK);
         if (!ok) break;
-        ptx::tc_fence_after_sync();
         issue_s(0, sK);
         ptx::mma_commit(ptx::smem_u32(&bars->s_full[0]));
         if (has1) {
@@ -349,15 +370,11 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
           ptx::mma_commit(ptx::smem_u32(&bars->s_full[1]));
         }
         ptx::mma_commit(ptx::smem_u32(&bars->kv_empty[sK]));
-        ++it;
         if (nkv == 1) ptx::mma_commit(ptx::smem_u32(&bars->q_empty));
 
         for (int j = 0; j < nkv && ok; ++j) {
-          const uint32_t sV = it % C::STAGES;
-          ok = bounded_wait(ptx::smem_u32(&bars->kv_full[sV]), (it / C::STAGES) & 1, bars,
-                            p.timeout_ns);
+          ok = take_stage(sV);
           if (!ok) break;
-          ++it;
           const bool has_next = j + 1 < nkv;
           // O0 += P0 V_j
           ok = bounded_wait(ptx::smem_u32(&bars->p_ready[0]), pc0 & 1, bars, p.timeout_ns);
@@ -368,11 +385,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
           if (!has_next) ptx::mma_commit(ptx::smem_u32(&bars->o_full[0]));
           // S0 for key block j+1 as soon as P0 has been consumed.
           if (has_next) {
-            sK = it % C::STAGES;
-            ok = bounded_wait(ptx::smem_u32(&bars->kv_full[sK]), (it / C::STAGES) & 1, bars,
-                              p.timeout_ns);
+            ok = take_stage(sK);
             if (!ok) break;
-            ptx::tc_fence_after_sync();
             issue_s(0, sK);
             ptx::mma_commit(ptx::smem_u32(&bars->s_full[0]));
           }
@@ -391,7 +405,6 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
               ptx::mma_commit(ptx::smem_u32(&bars->s_full[1]));
             }
             ptx::mma_commit(ptx::smem_u32(&bars->kv_empty[sK]));
-            ++it;
             if (j + 2 == nkv) ptx::mma_commit(ptx::smem_u32(&bars->q_empty));
           }
         }
