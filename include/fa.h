@@ -23,6 +23,8 @@
 #ifndef UNET_FA_FWD_GB300_FA_H
 #define UNET_FA_FWD_GB300_FA_H
 
+#include <stddef.h>
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -54,9 +56,9 @@ typedef enum {
  * A row whose keys are all masked gives O = 0 and LSE = -inf.
  *
  * Ownership: the caller owns every buffer; nothing is retained after the call
- * returns except a host-side cache of TMA descriptors keyed by pointer and
- * shape.  Every pointer must be 16-byte aligned (a TMA requirement); out and
- * lse must not overlap q, k, v, mask or each other.
+ * returns (TMA descriptors are encoded per call and passed by value).  Every
+ * pointer must be 16-byte aligned (a TMA requirement); out and lse must not
+ * overlap q, k, v, mask or each other.
  *
  * Errors: arguments are validated before any CUDA call; an invalid call
  * returns FA_ERR_INVALID_ARGUMENT or FA_ERR_UNSUPPORTED and launches nothing.
@@ -67,6 +69,46 @@ typedef enum {
  */
 int fa_fwd(const void* q, const void* k, const void* v, const float* mask, void* out, float* lse,
            int B, int H, int Nq, int Nk, int D, float scale, void* stream);
+
+/*
+ * fa_fwd_split — the same forward with the key axis cut into `num_splits`
+ * ranges computed by separate work units, then merged.
+ *
+ * Each range r yields its own normalised partial output O_r and LSE_r; the
+ * merge is exact: LSE = ln sum_r e^(LSE_r), O = sum_r e^(LSE_r - LSE) O_r.
+ * This is the exchange step of ring (sequence-parallel) attention in
+ * "FlashAttention原理与工业实战" §6.2, here on one GPU: it fills the SMs when
+ * B*H*ceil(Nq/256) work units are fewer than the SM count (few heads, short
+ * query sets, long key sets).
+ *
+ *   q, k, v, mask, out, lse, B, H, Nq, Nk, D, scale, stream: as in fa_fwd.
+ *   num_splits  >= 1 requested ranges; the library uses min(num_splits, nkv)
+ *               balanced ranges of whole 128-key blocks, nkv = ceil(Nk / 128).
+ *               1 behaves exactly as fa_fwd.
+ *   workspace   device scratch, 16-byte aligned, at least
+ *               fa_split_workspace_bytes(B, H, Nq, D, num_splits) bytes; holds
+ *               fp32 partial O [ranges][B*H][Nq][D] and LSE [ranges][B*H][Nq].
+ *               Owned by the caller; may be NULL when one range is used.  It
+ *               must not overlap any other buffer and must not be used by
+ *               another call in flight at the same time.
+ *
+ * Errors: as fa_fwd, plus FA_ERR_INVALID_ARGUMENT for num_splits < 1 or a
+ * missing, misaligned, too small or overlapping workspace.  Two kernels are
+ * enqueued on `stream` (the split forward, then the merge).
+ */
+int fa_fwd_split(const void* q, const void* k, const void* v, const float* mask, void* out,
+                 float* lse, int B, int H, int Nq, int Nk, int D, float scale, int num_splits,
+                 void* workspace, size_t workspace_bytes, void* stream);
+
+/* Workspace bytes fa_fwd_split needs for these sizes (0 for invalid sizes). */
+size_t fa_split_workspace_bytes(int B, int H, int Nq, int D, int num_splits);
+
+/*
+ * A key-range count for fa_fwd_split on a GPU with `num_sms` SMs: 1 when the
+ * unsplit work units already cover every SM, else enough ranges to do so,
+ * each range at least four 128-key blocks long.  Pure arithmetic; no CUDA call.
+ */
+int fa_split_count(int B, int H, int Nq, int Nk, int num_sms);
 
 /*
  * fa_read_device_status — read, and reset to FA_OK, the status word that

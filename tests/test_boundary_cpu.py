@@ -78,3 +78,34 @@ def test_valid_call_without_gpu_reports_cuda_error(lib):
 def test_fault_injection_hook(lib, monkeypatch):
     monkeypatch.setenv("FA_FAULT_INJECT", "launch")
     assert _call() == 3
+
+
+def test_split_workspace_and_count(lib):
+    assert fa.split_workspace_bytes(1, 24, 256, 128, 4) == (
+        ((24 * 256 * 4 * 128 * 4 + 255) // 256) * 256 + ((24 * 256 * 4 * 4 + 255) // 256) * 256)
+    assert fa.split_workspace_bytes(0, 1, 1, 64, 1) == 0
+    assert fa.split_workspace_bytes(1, 1, 1, 64, 0) == 0
+    # enough units already: no split
+    assert fa.split_count(1, 24, 16896, 16896, num_sms=152) == 1
+    # one head, 256 queries, 119056 keys (931 key blocks): fill 152 SMs
+    assert fa.split_count(1, 1, 256, 119056, num_sms=152) == 152
+    # short key set: at least four key blocks per range
+    assert fa.split_count(1, 1, 128, 1024, num_sms=152) == 2
+    assert fa.split_count(1, 1, 128, 100, num_sms=152) == 1
+
+
+def _split_call(**kw):
+    a = dict(FAKE, num_splits=4, ws=0x80000, ws_bytes=1 << 30)
+    a.update(kw)
+    return fa.load_library().fa_fwd_split(a["q"], a["k"], a["v"], a["mask"], a["out"], a["lse"],
+                                          a["B"], a["H"], a["Nq"], 1000, a["D"],
+                                          ctypes.c_float(a["scale"]), a["num_splits"], a["ws"],
+                                          a["ws_bytes"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(num_splits=0), 1), (dict(ws=None), 1), (dict(ws=0x80008), 1), (dict(ws_bytes=1024), 1),
+    (dict(D=48), 2), (dict(q=None), 1),
+])
+def test_split_validation_before_any_cuda_call(lib, kw, code):
+    assert _split_call(**kw) == code

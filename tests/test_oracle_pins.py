@@ -333,3 +333,31 @@ def test_thread_count_does_not_change_result():
     o1, l1 = oracle.attention(q, k, v, nthreads=1)
     o4, l4 = oracle.attention(q, k, v, nthreads=4)
     assert np.array_equal(o1, o4) and np.array_equal(l1, l4)
+
+
+# ---------------------------------------------------------------------------
+# Split-key merge: attention over disjoint key ranges, merged by the LSE rule,
+# equals attention over all keys (the exchange step of ring attention,
+# "FlashAttention原理与工业实战" §6.2) — exact up to rounding.
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("cuts", [[0, 40, 97], [0, 1, 2, 97], [0, 64, 65, 97], [0, 20, 50, 80, 97]])
+def test_split_key_merge_is_exact(cuts):
+    rng = _rng(13)
+    B, H, Nq, Nk, D = 2, 2, 9, 97, 16
+    q, k, v = _randn(rng, B, H, Nq, D), _randn(rng, B, H, Nk, D), _randn(rng, B, H, Nk, D)
+    mask = np.zeros((B, Nk), np.float32)
+    mask[1, 30:] = -np.inf          # batch 1: the later ranges are fully masked
+    mask[0, 5] = 1.25
+    o_full, l_full = oracle.attention(q, k, v, mask=mask, scale=0.3)
+    parts = []
+    for a, b in zip(cuts[:-1], cuts[1:]):
+        parts.append(oracle.attention(q, k[:, :, a:b].copy(), v[:, :, a:b].copy(),
+                                      mask=mask[:, a:b].copy(), scale=0.3))
+    lses = np.stack([l for _, l in parts])                 # [S, B, H, Nq]
+    m = lses.max(axis=0)
+    w = np.exp(lses - m)                                   # -inf ranges weigh 0
+    lse = m + np.log(w.sum(axis=0))
+    o = sum(wi[..., None] * oi for wi, (oi, _) in zip(w, parts)) / w.sum(axis=0)[..., None]
+    assert np.max(np.abs(o - o_full)) < 1e-12
+    assert np.max(np.abs(lse - l_full)) < 1e-12

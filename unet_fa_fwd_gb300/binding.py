@@ -43,6 +43,14 @@ def load_library() -> ctypes.CDLL:
             vp, i32, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
             lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp]
             lib.fa_fwd.restype = i32
+            sz = ctypes.c_size_t
+            lib.fa_fwd_split.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32,
+                                         vp, sz, vp]
+            lib.fa_fwd_split.restype = i32
+            lib.fa_split_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
+            lib.fa_split_workspace_bytes.restype = sz
+            lib.fa_split_count.argtypes = [i32, i32, i32, i32, i32]
+            lib.fa_split_count.restype = i32
             lib.fa_read_device_status.argtypes = [vp, ctypes.POINTER(i32)]
             lib.fa_read_device_status.restype = i32
             lib.fa_status_string.argtypes = [i32]
@@ -118,6 +126,61 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, mask: torch.Tensor | 
     out = torch.empty((B, H, Nq, D), dtype=torch.bfloat16, device=q.device)
     lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
     fa_fwd(q, k, v, mask, out, lse, scale=scale, stream=stream)
+    return out, lse
+
+
+def split_workspace_bytes(B: int, H: int, Nq: int, D: int, num_splits: int) -> int:
+    return int(load_library().fa_split_workspace_bytes(B, H, Nq, D, num_splits))
+
+
+def split_count(B: int, H: int, Nq: int, Nk: int, num_sms: int | None = None) -> int:
+    """Key-range count the library recommends for these sizes on this GPU."""
+    if num_sms is None:
+        num_sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    return int(load_library().fa_split_count(B, H, Nq, Nk, num_sms))
+
+
+def fa_fwd_split(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, mask: torch.Tensor | None,
+                 out: torch.Tensor, lse: torch.Tensor, num_splits: int,
+                 workspace: torch.Tensor | None, scale: float | None = None, stream=None) -> None:
+    """Split-key forward into caller buffers; `workspace` is a device tensor of at least
+    split_workspace_bytes(...) bytes (any dtype, contiguous), or None for one range."""
+    B, H, Nq, D = q.shape
+    Nk = k.shape[2]
+    _check(q, "q", torch.bfloat16, (B, H, Nq, D))
+    _check(k, "k", torch.bfloat16, (B, H, Nk, D))
+    _check(v, "v", torch.bfloat16, (B, H, Nk, D))
+    _check(out, "out", torch.bfloat16, (B, H, Nq, D))
+    _check(lse, "lse", torch.float32, (B, H, Nq))
+    if mask is not None:
+        _check(mask, "mask", torch.float32, (B, Nk))
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        if not workspace.is_cuda or not workspace.is_contiguous():
+            raise ValueError("workspace must be a contiguous CUDA tensor")
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    rc = load_library().fa_fwd_split(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                      None if mask is None else mask.data_ptr(), out.data_ptr(),
+                                      lse.data_ptr(), B, H, Nq, Nk, D, ctypes.c_float(scale),
+                                      int(num_splits), ws_ptr, ws_bytes, _stream_handle(stream))
+    if rc != FA_OK:
+        raise RuntimeError(f"fa_fwd_split failed: {status_string(rc)}")
+
+
+def fwd_split(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, mask: torch.Tensor | None = None,
+              scale: float | None = None, num_splits: int | None = None, stream=None):
+    """Allocate outputs and workspace (torch) and run the split-key forward."""
+    B, H, Nq, D = q.shape
+    Nk = k.shape[2]
+    if num_splits is None:
+        num_splits = split_count(B, H, Nq, Nk)
+    out = torch.empty((B, H, Nq, D), dtype=torch.bfloat16, device=q.device)
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    ws = torch.empty(split_workspace_bytes(B, H, Nq, D, num_splits), dtype=torch.uint8,
+                     device=q.device)
+    fa_fwd_split(q, k, v, mask, out, lse, num_splits, ws, scale=scale, stream=stream)
     return out, lse
 
 

@@ -123,12 +123,24 @@ int launch(const fa::Params& prm, DeviceState& st, int slot, cudaStream_t stream
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
-}  // namespace
 
-extern "C" {
+int launch_merge(const float* part_o, const float* part_lse, __nv_bfloat16* out, float* lse,
+                 int splits, long long rows, int D, cudaStream_t s) {
+  const int rows_per_block = 256 / 32;
+  const long long blocks = (rows + rows_per_block - 1) / rows_per_block;
+  if (blocks > INT_MAX) return FA_ERR_INVALID_ARGUMENT;
+  switch (D) {
+    case 32: fa::fa_merge_kernel<32><<<(int)blocks, 256, 0, s>>>(part_o, part_lse, out, lse, splits, rows); break;
+    case 64: fa::fa_merge_kernel<64><<<(int)blocks, 256, 0, s>>>(part_o, part_lse, out, lse, splits, rows); break;
+    default: fa::fa_merge_kernel<128><<<(int)blocks, 256, 0, s>>>(part_o, part_lse, out, lse, splits, rows); break;
+  }
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
 
-int fa_fwd(const void* q, const void* k, const void* v, const float* mask, void* out, float* lse,
-           int B, int H, int Nq, int Nk, int D, float scale, void* stream) {
+// Validation and set-up shared by the entry points.  On success `prm` holds
+// the tensor maps and sizes of an unsplit launch and `st` the device state.
+int prepare(const void* q, const void* k, const void* v, const float* mask, void* out, float* lse,
+            int B, int H, int Nq, int Nk, int D, float scale, fa::Params* prm, DeviceState** st) {
   // ---- validation: no CUDA call before this block passes ----
   if (!q || !k || !v || !out || !lse) return FA_ERR_INVALID_ARGUMENT;
   if (B < 1 || H < 1 || Nq < 1 || Nk < 1) return FA_ERR_INVALID_ARGUMENT;
@@ -156,35 +168,112 @@ int fa_fwd(const void* q, const void* k, const void* v, const float* mask, void*
     return FA_ERR_CUDA;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
-  DeviceState* st = nullptr;
-  int rc = device_setup(dev, &st);
+  int rc = device_setup(dev, st);
   if (rc != FA_OK) return rc;
-  if (!st->supported) return FA_ERR_UNSUPPORTED;
+  if (!(*st)->supported) return FA_ERR_UNSUPPORTED;
 
-  fa::Params prm;
-  std::memset(&prm, 0, sizeof(prm));
-  if (encode_map(&prm.tm_q, q, (int)BH, Nq, D) != FA_OK ||
-      encode_map(&prm.tm_k, k, (int)BH, Nk, D) != FA_OK ||
-      encode_map(&prm.tm_v, v, (int)BH, Nk, D) != FA_OK)
+  std::memset(prm, 0, sizeof(*prm));
+  if (encode_map(&prm->tm_q, q, (int)BH, Nq, D) != FA_OK ||
+      encode_map(&prm->tm_k, k, (int)BH, Nk, D) != FA_OK ||
+      encode_map(&prm->tm_v, v, (int)BH, Nk, D) != FA_OK)
     return FA_ERR_CUDA;
-  prm.out = reinterpret_cast<__nv_bfloat16*>(out);
-  prm.lse = lse;
-  prm.mask = mask;
-  prm.H = H;
-  prm.Nq = Nq;
-  prm.Nk = Nk;
-  prm.units_per_bh = (int)upb;
-  prm.num_units = (int)(BH * upb);
-  prm.nkv = (Nk + 127) / 128;
-  prm.scale_log2 = (float)((double)scale * 1.4426950408889634);
-  prm.timeout_ns = timeout_ns_from_env();
+  prm->out = reinterpret_cast<__nv_bfloat16*>(out);
+  prm->lse = lse;
+  prm->mask = mask;
+  prm->H = H;
+  prm->Nq = Nq;
+  prm->Nk = Nk;
+  prm->BH = (int)BH;
+  prm->units_per_bh = (int)upb;
+  prm->nkv = (Nk + 127) / 128;
+  prm->num_splits = 1;
+  prm->num_units = (int)(BH * upb);
+  prm->scale_log2 = (float)((double)scale * 1.4426950408889634);
+  prm->timeout_ns = timeout_ns_from_env();
+  return FA_OK;
+}
 
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+int launch_fwd(const fa::Params& prm, DeviceState& st, int D, cudaStream_t s) {
   switch (D) {
-    case 32: return launch<32>(prm, *st, 0, s);
-    case 64: return launch<64>(prm, *st, 1, s);
-    default: return launch<128>(prm, *st, 2, s);
+    case 32: return launch<32>(prm, st, 0, s);
+    case 64: return launch<64>(prm, st, 1, s);
+    default: return launch<128>(prm, st, 2, s);
   }
+}
+
+// Key ranges actually used for a requested count: at most one per key block,
+// so that every range is non-empty.
+int effective_splits(int nkv, int requested) { return requested < nkv ? requested : nkv; }
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+}  // namespace
+
+extern "C" {
+
+int fa_fwd(const void* q, const void* k, const void* v, const float* mask, void* out, float* lse,
+           int B, int H, int Nq, int Nk, int D, float scale, void* stream) {
+  fa::Params prm;
+  DeviceState* st = nullptr;
+  const int rc = prepare(q, k, v, mask, out, lse, B, H, Nq, Nk, D, scale, &prm, &st);
+  if (rc != FA_OK) return rc;
+  return launch_fwd(prm, *st, D, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t fa_split_workspace_bytes(int B, int H, int Nq, int D, int num_splits) {
+  if (B < 1 || H < 1 || Nq < 1 || D < 1 || num_splits < 1) return 0;
+  const size_t rows = (size_t)B * H * Nq * num_splits;
+  return align256(rows * D * sizeof(float)) + align256(rows * sizeof(float));
+}
+
+int fa_split_count(int B, int H, int Nq, int Nk, int num_sms) {
+  if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || num_sms < 1) return 1;
+  const long long units = (long long)B * H * ((((long long)Nq + 127) / 128 + 1) / 2);
+  const int nkv = (Nk + 127) / 128;
+  if (units >= num_sms) return 1;
+  // Enough ranges to fill every SM once, each range at least 4 key blocks long.
+  long long want = (num_sms + units - 1) / units;
+  const long long most = nkv / 4 > 1 ? nkv / 4 : 1;
+  if (want > most) want = most;
+  if (want > 256) want = 256;
+  return effective_splits(nkv, (int)want);
+}
+
+int fa_fwd_split(const void* q, const void* k, const void* v, const float* mask, void* out,
+                 float* lse, int B, int H, int Nq, int Nk, int D, float scale, int num_splits,
+                 void* workspace, size_t workspace_bytes, void* stream) {
+  if (num_splits < 1) return FA_ERR_INVALID_ARGUMENT;
+  const int nkv = Nk > 0 ? (Nk + 127) / 128 : 1;
+  const int splits = effective_splits(nkv, num_splits);
+  if (splits > 1) {
+    if (!workspace || !aligned16(workspace)) return FA_ERR_INVALID_ARGUMENT;
+    if (workspace_bytes < fa_split_workspace_bytes(B, H, Nq, D, splits)) return FA_ERR_INVALID_ARGUMENT;
+  }
+  fa::Params prm;
+  DeviceState* st = nullptr;
+  int rc = prepare(q, k, v, mask, out, lse, B, H, Nq, Nk, D, scale, &prm, &st);
+  if (rc != FA_OK) return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (splits == 1) return launch_fwd(prm, *st, D, s);
+
+  const size_t rows = (size_t)prm.BH * Nq;
+  const size_t o_bytes = align256(rows * splits * D * sizeof(float));
+  if (ranges_overlap(workspace, workspace_bytes, q, (size_t)prm.BH * Nq * D * 2) ||
+      ranges_overlap(workspace, workspace_bytes, k, (size_t)prm.BH * Nk * D * 2) ||
+      ranges_overlap(workspace, workspace_bytes, v, (size_t)prm.BH * Nk * D * 2) ||
+      ranges_overlap(workspace, workspace_bytes, out, rows * D * 2) ||
+      ranges_overlap(workspace, workspace_bytes, lse, rows * 4) ||
+      ranges_overlap(workspace, workspace_bytes, mask, mask ? (size_t)B * Nk * 4 : 0))
+    return FA_ERR_INVALID_ARGUMENT;
+  prm.num_splits = splits;
+  prm.num_units *= splits;
+  prm.part_o = reinterpret_cast<float*>(workspace);
+  prm.part_lse = reinterpret_cast<float*>(reinterpret_cast<char*>(workspace) + o_bytes);
+  if (prm.num_units < 0 || (long long)prm.BH * prm.units_per_bh * splits > INT_MAX)
+    return FA_ERR_INVALID_ARGUMENT;
+  rc = launch_fwd(prm, *st, D, s);
+  if (rc != FA_OK) return rc;
+  return launch_merge(prm.part_o, prm.part_lse, prm.out, lse, splits, (long long)rows, D, s);
 }
 
 int fa_read_device_status(void* stream, int* status) {

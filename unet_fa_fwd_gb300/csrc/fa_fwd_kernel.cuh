@@ -87,13 +87,35 @@ struct Params {  // 64-byte aligned through its CUtensorMap members
   __nv_bfloat16* out;  // [BH][Nq][D]
   float* lse;          // [BH][Nq]
   const float* mask;   // [B][Nk] or nullptr
-  int H, Nq, Nk;
-  int num_units;       // BH * units_per_bh
+  int H, Nq, Nk, BH;
+  int num_units;       // BH * units_per_bh * num_splits
   int units_per_bh;    // ceil(ceil(Nq/128)/2)
-  int nkv;             // ceil(Nk/128)
+  int nkv;             // ceil(Nk/128): key blocks in all
+  int num_splits;      // key ranges computed separately (1 = no split), <= nkv
+  float* part_o;       // split mode: fp32 [num_splits][BH][Nq][D] partial O (else nullptr)
+  float* part_lse;     // split mode: fp32 [num_splits][BH][Nq] partial LSE
   float scale_log2;    // scale * log2(e)
   unsigned long long timeout_ns;
 };
+
+// One work unit: 256 query rows of one (b, h) against one range of key blocks.
+struct Unit {
+  int bh, q0, split, tile0, ntiles;
+};
+
+// Units are numbered head-major, then query pair, then key range, so CTAs
+// running together share a head's K/V (and Q) in L2.
+__device__ __forceinline__ Unit decode_unit(const Params& p, int u) {
+  Unit r;
+  r.split = u % p.num_splits;
+  const int rest = u / p.num_splits;
+  r.bh = rest / p.units_per_bh;
+  r.q0 = (rest % p.units_per_bh) * 256;
+  // Balanced ranges: range s covers key blocks [s*nkv/S, (s+1)*nkv/S).
+  r.tile0 = (int)((long long)r.split * p.nkv / p.num_splits);
+  r.ntiles = (int)((long long)(r.split + 1) * p.nkv / p.num_splits) - r.tile0;
+  return r;
+}
 
 // Shared-memory matrix descriptor (tcgen05 "matrix descriptor"): start
 // address, leading / stride byte offsets (16-byte units), version 1,
@@ -248,8 +270,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       uint32_t q_issued = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uc) {
-        const int bh = u / p.units_per_bh;
-        const int q0 = (u % p.units_per_bh) * 256;
+        const Unit un = decode_unit(p, u);
+        const int bh = un.bh, q0 = un.q0;
         const int ntiles = (q0 + 128 < p.Nq) ? 2 : 1;
         ok = bounded_wait(ptx::smem_u32(&bars->q_empty), (uc & 1) ^ 1, bars, p.timeout_ns);
         if (!ok) break;
@@ -260,7 +282,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
             ptx::tma_load_3d(ptx::smem_u32(sQ + t * C::TILE_BYTES + c * C::CHUNK_BYTES), &p.tm_q,
                              qbar, c * C::CHUNK_ELEMS, q0 + t * 128, bh);
         ++q_issued;
-        for (int j = 0; j < p.nkv && ok; ++j) {
+        for (int j = 0; j < un.ntiles && ok; ++j) {
           for (int kv = 0; kv < 2; ++kv, ++it) {
             const uint32_t s = it % C::STAGES;
             const uint32_t ph = (it / C::STAGES) & 1;
@@ -271,7 +293,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
             const void* tm = kv == 0 ? (const void*)&p.tm_k : (const void*)&p.tm_v;
             for (int c = 0; c < C::NCHUNK; ++c)
               ptx::tma_load_3d(ptx::smem_u32(sRing + s * C::TILE_BYTES + c * C::CHUNK_BYTES), tm,
-                               fb, c * C::CHUNK_ELEMS, j * 128, bh);
+                               fb, c * C::CHUNK_ELEMS, (un.tile0 + j) * 128, bh);
             ++issued[s];
           }
         }
@@ -353,9 +375,9 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       };
 
       for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uc) {
-        const int q0 = (u % p.units_per_bh) * 256;
-        const bool has1 = q0 + 128 < p.Nq;
-        const int nkv = p.nkv;
+        const Unit un = decode_unit(p, u);
+        const bool has1 = un.q0 + 128 < p.Nq;
+        const int nkv = un.ntiles;
         ok = bounded_wait(ptx::smem_u32(&bars->q_full), uc & 1, bars, p.timeout_ns);
         if (!ok) break;
         ptx::tc_fence_after_sync();
@@ -442,15 +464,15 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     bool ok = true;
 
     for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
-      const int bh = u / p.units_per_bh;
-      const int q0 = (u % p.units_per_bh) * 256;
+      const Unit un = decode_unit(p, u);
+      const int bh = un.bh, q0 = un.q0;
       if (t == 1 && !(q0 + 128 < p.Nq)) continue;
       const int qrow = q0 + t * 128 + row;
       const float* mask_b = p.mask ? p.mask + (size_t)(bh / p.H) * p.Nk : nullptr;
       float m = -INFINITY;  // running max of t_ij (log2 domain)
       float l = 0.f;        // running denominator relative to m
 
-      for (int j = 0; j < p.nkv; ++j) {
+      for (int j = 0; j < un.ntiles; ++j) {
         ok = bounded_wait_warp(bar_s, sc & 1, bars, p.timeout_ns);
         if (!ok) break;
         ++sc;
@@ -462,7 +484,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
 #pragma unroll
           for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(r[c]);
         }
-        const int kbase = j * 128;
+        const int kbase = (un.tile0 + j) * 128;
         // Fast path: full key block, no mask, non-negative scale — the row max
         // is taken on raw scores and scaled once.  Otherwise scores are
         // materialised in the log2 domain with the mask and the Nk tail.
@@ -566,32 +588,94 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       ptx::tc_fence_after_sync();
       const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
       const bool valid_row = qrow < p.Nq;
-      __nv_bfloat16* orow = p.out + ((size_t)bh * p.Nq + (valid_row ? qrow : 0)) * D;
+      constexpr float kLn2 = 0.6931471805599453f;
+      const float row_lse = (l > 0.f) ? (m + __log2f(l)) * kLn2 : -INFINITY;
+      if (p.part_o == nullptr) {
+        __nv_bfloat16* orow = p.out + ((size_t)bh * p.Nq + (valid_row ? qrow : 0)) * D;
 #pragma unroll
-      for (int cb = 0; cb < D; cb += 32) {
-        uint32_t r[32];
-        ptx::tmem_ld32x32b_x32(tO + cb, r);
-        uint32_t packed[16];
+        for (int cb = 0; cb < D; cb += 32) {
+          uint32_t r[32];
+          ptx::tmem_ld32x32b_x32(tO + cb, r);
+          uint32_t packed[16];
 #pragma unroll
-        for (int c = 0; c < 32; c += 2)
-          packed[c / 2] = ptx::pack_bf16x2(__uint_as_float(r[c]) * inv_l,
-                                           __uint_as_float(r[c + 1]) * inv_l);
-        if (valid_row) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + cb);
+          for (int c = 0; c < 32; c += 2)
+            packed[c / 2] = ptx::pack_bf16x2(__uint_as_float(r[c]) * inv_l,
+                                             __uint_as_float(r[c + 1]) * inv_l);
+          if (valid_row) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + cb);
 #pragma unroll
-          for (int v4 = 0; v4 < 4; ++v4)
-            dst[v4] = make_uint4(packed[4 * v4], packed[4 * v4 + 1], packed[4 * v4 + 2],
-                                 packed[4 * v4 + 3]);
+            for (int v4 = 0; v4 < 4; ++v4)
+              dst[v4] = make_uint4(packed[4 * v4], packed[4 * v4 + 1], packed[4 * v4 + 2],
+                                   packed[4 * v4 + 3]);
+          }
         }
-      }
-      if (valid_row) {
-        constexpr float kLn2 = 0.6931471805599453f;
-        p.lse[(size_t)bh * p.Nq + qrow] = (l > 0.f) ? (m + __log2f(l)) * kLn2 : -INFINITY;
+        if (valid_row) p.lse[(size_t)bh * p.Nq + qrow] = row_lse;
+      } else {
+        // Split mode: this key range's normalised O (fp32) and its LSE, merged
+        // by fa_merge_kernel.
+        const size_t prow = ((size_t)un.split * p.BH + bh) * p.Nq + (valid_row ? qrow : 0);
+        float* orow = p.part_o + prow * D;
+#pragma unroll
+        for (int cb = 0; cb < D; cb += 32) {
+          uint32_t r[32];
+          ptx::tmem_ld32x32b_x32(tO + cb, r);
+          if (valid_row) {
+            float4* dst = reinterpret_cast<float4*>(orow + cb);
+#pragma unroll
+            for (int v4 = 0; v4 < 8; ++v4)
+              dst[v4] = make_float4(__uint_as_float(r[4 * v4]) * inv_l,
+                                    __uint_as_float(r[4 * v4 + 1]) * inv_l,
+                                    __uint_as_float(r[4 * v4 + 2]) * inv_l,
+                                    __uint_as_float(r[4 * v4 + 3]) * inv_l);
+          }
+        }
+        if (valid_row) p.part_lse[prow] = row_lse;
       }
     }
     ptx::tc_fence_before_sync();
   }
   finish();  // softmax warps 0-7
+}
+
+// Merge of per-key-range results (the exchange step of ring attention, done
+// on one GPU): for each row, LSE = log sum_s e^(LSE_s) and
+// O = sum_s e^(LSE_s - LSE) O_s.  One warp per row, D/32 columns per lane;
+// memory bound (reads num_splits * (D + 1) fp32 per row).
+template <int D>
+__global__ void __launch_bounds__(256) fa_merge_kernel(const float* __restrict__ part_o,
+                                                       const float* __restrict__ part_lse,
+                                                       __nv_bfloat16* __restrict__ out,
+                                                       float* __restrict__ lse, int num_splits,
+                                                       long long rows) {
+  constexpr int PER = D / 32;
+  const long long row = (long long)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  if (row >= rows) return;
+  float mx = -INFINITY;
+  for (int s = 0; s < num_splits; ++s) mx = fmaxf(mx, __ldg(part_lse + (long long)s * rows + row));
+  float acc[PER];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) acc[i] = 0.f;
+  float wsum = 0.f;
+  if (mx != -INFINITY) {
+    for (int s = 0; s < num_splits; ++s) {
+      const float w = __expf(__ldg(part_lse + (long long)s * rows + row) - mx);
+      wsum += w;
+      const float* src = part_o + ((long long)s * rows + row) * D + lane * PER;
+#pragma unroll
+      for (int i = 0; i < PER; ++i) acc[i] = fmaf(w, __ldg(src + i), acc[i]);
+    }
+  }
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+  __nv_bfloat16* dst = out + row * D + lane * PER;
+  if constexpr (PER == 1) {
+    dst[0] = __float2bfloat16_rn(acc[0] * inv);
+  } else {
+#pragma unroll
+    for (int i = 0; i < PER; i += 2)
+      *reinterpret_cast<uint32_t*>(dst + i) = ptx::pack_bf16x2(acc[i] * inv, acc[i + 1] * inv);
+  }
+  if (lane == 0) lse[row] = (wsum > 0.f) ? mx + __logf(wsum) : -INFINITY;
 }
 
 }  // namespace fa
