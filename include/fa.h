@@ -110,6 +110,33 @@ size_t fa_split_workspace_bytes(int B, int H, int Nq, int D, int num_splits);
  */
 int fa_split_count(int B, int H, int Nq, int Nk, int num_sms);
 
+/* Bytes of the fixed device scratch that fa_fwd_split_noalloc uses. */
+#define FA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+/*
+ * fa_fwd_split_noalloc — fa_fwd_split for callers that cannot allocate device
+ * memory (a plugin whose host application owns every device allocation, or a
+ * latency-critical path that cannot afford cudaMalloc's implicit device
+ * synchronisation).  The pages have no counterpart of this entry point.
+ *
+ * Arguments as fa_fwd_split, without the workspace: the partial results live
+ * in a fixed array of FA_NOALLOC_SCRATCH_BYTES inside the library, which every
+ * GPU that loads the library holds until the process exits.  The call
+ * allocates nothing (no cudaMalloc, cudaFree or allocating library routine).
+ * Sizes whose workspace (fa_split_workspace_bytes with the range count used)
+ * exceeds FA_NOALLOC_SCRATCH_BYTES are rejected with FA_ERR_INVALID_ARGUMENT
+ * before anything is enqueued.
+ *
+ * The first call on each device looks up the array's device address (with
+ * that device current) and caches it; make that first call before capturing
+ * a stream.  All calls on a device share the one array, which keeps the last
+ * call's contents: calls that overlap on the GPU (other streams, or before the
+ * previous call finished) race on it and must be serialised by the caller.
+ */
+int fa_fwd_split_noalloc(const void* q, const void* k, const void* v, const float* mask, void* out,
+                         float* lse, int B, int H, int Nq, int Nk, int D, float scale,
+                         int num_splits, void* stream);
+
 /*
  * fa_read_device_status — read, and reset to FA_OK, the status word that
  * kernels on the current device write when an internal wait times out.

@@ -276,6 +276,48 @@ int fa_fwd_split(const void* q, const void* k, const void* v, const float* mask,
   return launch_merge(prm.part_o, prm.part_lse, prm.out, lse, splits, (long long)rows, D, s);
 }
 
+// ---------------------------------------------------------------------------
+// fa_fwd_split_noalloc: the split-key forward for callers that must not
+// allocate device memory — for example a plugin inside a host application
+// that owns every device allocation, or a latency-critical path where
+// cudaMalloc (which can synchronise the device) is not acceptable.  Its
+// scratch is a fixed array inside this library.  A __device__ array's name in
+// host code is only a host-side stand-in, so its device address is looked up
+// with cudaGetSymbolAddress, once per device, with that device current; that
+// look-up happens on the first call on each device.
+// ---------------------------------------------------------------------------
+namespace {
+__device__ __align__(256) unsigned char g_noalloc_scratch[FA_NOALLOC_SCRATCH_BYTES];
+void* g_noalloc_scratch_addr[kMaxDevices] = {};
+}  // namespace
+
+int fa_fwd_split_noalloc(const void* q, const void* k, const void* v, const float* mask, void* out,
+                         float* lse, int B, int H, int Nq, int Nk, int D, float scale,
+                         int num_splits, void* stream) {
+  if (num_splits < 1 || Nk < 1) return FA_ERR_INVALID_ARGUMENT;
+  const int splits = effective_splits((Nk + 127) / 128, num_splits);
+  const size_t need = splits > 1 ? fa_split_workspace_bytes(B, H, Nq, D, splits) : 0;
+  if (splits > 1 && (need == 0 || need > (size_t)FA_NOALLOC_SCRATCH_BYTES))
+    return FA_ERR_INVALID_ARGUMENT;  // does not fit the fixed scratch (or bad sizes)
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
+  void* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!g_noalloc_scratch_addr[dev]) {
+      void* addr = nullptr;
+      if (cudaGetSymbolAddress(&addr, g_noalloc_scratch) != cudaSuccess || addr == nullptr)
+        return FA_ERR_CUDA;
+      g_noalloc_scratch_addr[dev] = addr;
+    }
+    scratch = g_noalloc_scratch_addr[dev];
+  }
+  // Every partial result the merge reads is written first by the forward, so
+  // nothing in the scratch needs clearing between calls.
+  return fa_fwd_split(q, k, v, mask, out, lse, B, H, Nq, Nk, D, scale, splits, scratch,
+                      (size_t)FA_NOALLOC_SCRATCH_BYTES, stream);
+}
+
 int fa_read_device_status(void* stream, int* status) {
   if (!status) return FA_ERR_INVALID_ARGUMENT;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
