@@ -40,6 +40,9 @@ def _load():
         lib.fa_oracle_rows.argtypes = [vp, vp, vp, vp, i32, vp, i32, dp, dp, i32, i32, i32, i32, i32,
                                        f64, i32]
         lib.fa_oracle_rows.restype = i32
+        lib.fa_oracle_fwd_ex.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, vp, i32, dp, dp, i32,
+                                         i32, i32, i32, i32, f64, i32]
+        lib.fa_oracle_fwd_ex.restype = i32
         lib.fa_oracle_probs.argtypes = [vp, vp, vp, i32, i32, i32, i32, dp, i32, i32, i32, i32, i32, f64]
         lib.fa_oracle_probs.restype = i32
         _lib = lib
@@ -116,6 +119,46 @@ def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, mask: np.ndarray | No
                                 out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
                                 lse.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
                                 B, H, Nq, Nk, D, float(scale), int(nthreads))
+    if rc != 0:
+        raise RuntimeError(f"oracle failed with code {rc}")
+    return out, lse
+
+
+def attention_ex(q: np.ndarray, k: np.ndarray, v: np.ndarray, mask: np.ndarray | None = None,
+                 full_mask: np.ndarray | None = None, causal: bool = False,
+                 scale: float | None = None, rows: np.ndarray | None = None,
+                 nthreads: int | None = None):
+    """fp64 forward with general masking.
+
+    mask: key-padding fp32 [B,Nk]; full_mask: additive fp32 [B, 1|H, Nq, Nk];
+    causal: exclude key j > query i.  Other arguments as attention().
+    """
+    lib = _load()
+    B, H, Nq, D = q.shape
+    Nk = k.shape[2]
+    qa, dt = _as_input(q)
+    ka, _ = _as_input(k)
+    va, _ = _as_input(v)
+    m = None if mask is None else np.ascontiguousarray(mask, dtype=np.float32)
+    fm, mh = None, 1
+    if full_mask is not None:
+        fm = np.ascontiguousarray(full_mask, dtype=np.float32)
+        if fm.ndim != 4 or fm.shape[0] != B or fm.shape[2:] != (Nq, Nk) or fm.shape[1] not in (1, H):
+            raise ValueError(f"full_mask must be [B, 1|H, Nq, Nk], got {fm.shape}")
+        mh = fm.shape[1]
+    if scale is None:
+        scale = 1.0 / np.sqrt(D)
+    r, nrows = None, Nq
+    if rows is not None:
+        r = np.ascontiguousarray(rows, dtype=np.int64)
+        nrows = r.shape[1]
+    out = np.empty((B, H, nrows, D), dtype=np.float64)
+    lse = np.empty((B, H, nrows), dtype=np.float64)
+    rc = lib.fa_oracle_fwd_ex(_ptr(qa), _ptr(ka), _ptr(va), _ptr(m), _ptr(fm), mh, int(bool(causal)),
+                              dt, _ptr(r), nrows if r is not None else 0,
+                              out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
+                              lse.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
+                              B, H, Nq, Nk, D, float(scale), int(nthreads or default_threads()))
     if rc != 0:
         raise RuntimeError(f"oracle failed with code {rc}")
     return out, lse

@@ -27,6 +27,12 @@
  *  - "FlashAttention原理与工业实战" §2.3 kernel signature: the forward also
  *    writes a per-row Lse; its base is not stated, the natural log is used.
  *
+ * General masking (fa_oracle_fwd_ex): an additive mask per (query, key) pair,
+ * [B, 1 or H, Nq, Nk], added after the scale like the key-padding mask; a
+ * boolean mask (keep where nonzero) is the additive mask 0 / -inf, as in
+ * "FlashAttention原理与工业实战" §2.1; causal excludes key j > query i (the
+ * lower-triangular mask of that page's §4.3 causal example, top-left aligned).
+ *
  * Readings where the pages are silent:
  *  - the mask is an additive fp32 key-padding mask of shape [B, Nk], broadcast
  *    over heads and query rows; it is not multiplied by `scale`;
@@ -66,6 +72,9 @@ typedef struct {
     const void* k;
     const void* v;
     const float* mask; /* [B, Nk] or NULL */
+    const float* full_mask; /* [B, mask_heads, Nq, Nk] additive, or NULL */
+    int mask_heads;         /* 1 (broadcast over heads) or H */
+    int causal;             /* key j > query i is excluded */
     int dtype;
     int B, H, Nq, Nk, D;
     double scale;
@@ -95,6 +104,11 @@ static void attend_one_row(const oracle_job* job, int64_t bh, int64_t i, double*
         }
         double sij = job->scale * dot;
         if (job->mask) sij += (double)job->mask[b * Nk + j];
+        if (job->full_mask) {
+            const int64_t hm = job->mask_heads == 1 ? 0 : bh % job->H;
+            sij += (double)job->full_mask[((b * job->mask_heads + hm) * Nq + i) * Nk + j];
+        }
+        if (job->causal && j > i) sij = -INFINITY;
         s[j] = sij;
     }
 
@@ -185,8 +199,31 @@ int fa_oracle_fwd(const void* q, const void* k, const void* v, const float* mask
                   int nthreads) {
     if (!q || !k || !v || !out || !lse || check_shape(B, H, Nq, Nk, D)) return 1;
     if (dtype != ORACLE_DTYPE_F32 && dtype != ORACLE_DTYPE_BF16) return 1;
-    oracle_job job = {q, k, v, mask, dtype, B, H, Nq, Nk, D, scale, NULL, 0, out, lse,
+    oracle_job job = {q, k, v, mask, NULL, 1, 0, dtype, B, H, Nq, Nk, D, scale, NULL, 0, out, lse,
                       (int64_t)B * H * Nq, 0};
+    return run_job(&job, nthreads);
+}
+
+/* Forward with general masking: the key-padding mask [B, Nk] (or NULL), an
+ * additive mask over every (query, key) pair [B, mask_heads, Nq, Nk] (or
+ * NULL; mask_heads 1 broadcasts over heads), and `causal` (key j excluded
+ * for query i when j > i, the top-left-aligned triangle).  `rows` NULL
+ * computes every row, else the rows[B*H*nrows] query indices per head. */
+int fa_oracle_fwd_ex(const void* q, const void* k, const void* v, const float* mask,
+                     const float* full_mask, int mask_heads, int causal, int dtype,
+                     const int64_t* rows, int nrows, double* out, double* lse, int B, int H,
+                     int Nq, int Nk, int D, double scale, int nthreads) {
+    if (!q || !k || !v || !out || !lse || check_shape(B, H, Nq, Nk, D)) return 1;
+    if (dtype != ORACLE_DTYPE_F32 && dtype != ORACLE_DTYPE_BF16) return 1;
+    if (full_mask && mask_heads != 1 && mask_heads != H) return 1;
+    if (rows) {
+        if (nrows < 1) return 1;
+        for (int64_t t = 0; t < (int64_t)B * H * nrows; ++t)
+            if (rows[t] < 0 || rows[t] >= Nq) return 1;
+    }
+    oracle_job job = {q, k, v, mask, full_mask, mask_heads < 1 ? 1 : mask_heads, causal ? 1 : 0,
+                      dtype, B, H, Nq, Nk, D, scale, rows, rows ? nrows : 0, out, lse,
+                      (int64_t)B * H * (rows ? nrows : Nq), 0};
     return run_job(&job, nthreads);
 }
 
@@ -200,8 +237,8 @@ int fa_oracle_rows(const void* q, const void* k, const void* v, const float* mas
     if (dtype != ORACLE_DTYPE_F32 && dtype != ORACLE_DTYPE_BF16) return 1;
     for (int64_t t = 0; t < (int64_t)B * H * nrows; ++t)
         if (rows[t] < 0 || rows[t] >= Nq) return 1;
-    oracle_job job = {q, k, v, mask, dtype, B, H, Nq, Nk, D, scale, rows, nrows, out, lse,
-                      (int64_t)B * H * nrows, 0};
+    oracle_job job = {q, k, v, mask, NULL, 1, 0, dtype, B, H, Nq, Nk, D, scale, rows, nrows, out,
+                      lse, (int64_t)B * H * nrows, 0};
     return run_job(&job, nthreads);
 }
 

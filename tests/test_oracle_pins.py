@@ -361,3 +361,77 @@ def test_split_key_merge_is_exact(cuts):
     o = sum(wi[..., None] * oi for wi, (oi, _) in zip(w, parts)) / w.sum(axis=0)[..., None]
     assert np.max(np.abs(o - o_full)) < 1e-12
     assert np.max(np.abs(lse - l_full)) < 1e-12
+
+
+# ---------------------------------------------------------------------------
+# General masks and causal (the oracle's fa_oracle_fwd_ex).
+# ---------------------------------------------------------------------------
+
+def test_full_mask_broadcast_of_key_padding_is_the_same_function():
+    rng = _rng(20)
+    B, H, Nq, Nk, D = 2, 3, 7, 19, 8
+    q, k, v = _randn(rng, B, H, Nq, D), _randn(rng, B, H, Nk, D), _randn(rng, B, H, Nk, D)
+    kp = np.where(rng.random((B, Nk)) < 0.3, -np.inf, 0.0).astype(np.float32)
+    kp[:, 0] = 0.5
+    full = np.broadcast_to(kp[:, None, None, :], (B, 1, Nq, Nk)).copy()
+    o1, l1 = oracle.attention(q, k, v, mask=kp)
+    o2, l2 = oracle.attention_ex(q, k, v, full_mask=full)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+def test_causal_closed_forms():
+    """Causal (key j <= query i): row 0 sees only key 0, so O_0 = V_0 and
+    LSE_0 = s_00; with q = 0 row i is the mean of V_0..V_i, LSE = ln(i+1)."""
+    rng = _rng(21)
+    B, H, N, D = 1, 2, 12, 8
+    q, k, v = _randn(rng, B, H, N, D), _randn(rng, B, H, N, D), _randn(rng, B, H, N, D)
+    o, l = oracle.attention_ex(q, k, v, causal=True, scale=0.5)
+    assert np.array_equal(o[:, :, 0], v[:, :, 0].astype(np.float64))
+    s00 = 0.5 * np.einsum("bhd,bhd->bh", q[:, :, 0].astype(np.float64), k[:, :, 0].astype(np.float64))
+    assert np.max(np.abs(l[:, :, 0] - s00)) < 1e-12
+    q0 = np.zeros_like(q)
+    o, l = oracle.attention_ex(q0, k, v, causal=True)
+    for i in range(N):
+        assert np.max(np.abs(o[:, :, i] - v[:, :, :i + 1].astype(np.float64).mean(axis=2))) < 1e-12
+        assert np.max(np.abs(l[:, :, i] - np.log(i + 1))) < 1e-12
+
+
+@pytest.mark.parametrize("heads", [1, 3])
+def test_general_masks_against_library_sdpa(heads):
+    """torch fp64 SDPA (a library routine) with an additive [B,heads,Nq,Nk]
+    mask, a boolean mask (keep = True) and is_causal."""
+    rng = _rng(22 + heads)
+    B, H, Nq, Nk, D = 2, 3, 11, 11, 16
+    q, k, v = _randn(rng, B, H, Nq, D), _randn(rng, B, H, Nk, D), _randn(rng, B, H, Nk, D)
+    add = (rng.standard_normal((B, heads, Nq, Nk)) * 2).astype(np.float32)
+    keep = rng.random((B, heads, Nq, Nk)) > 0.3
+    keep[..., 0] = True
+    tq, tk, tv = (torch.from_numpy(x).double() for x in (q, k, v))
+    # additive
+    o, l = oracle.attention_ex(q, k, v, full_mask=add, scale=0.4)
+    ref = F.scaled_dot_product_attention(tq, tk, tv, attn_mask=torch.from_numpy(add).double(), scale=0.4)
+    assert np.max(np.abs(o - ref.numpy())) < 1e-12
+    # boolean: masked_fill(mask == 0, -inf) is the additive 0 / -inf mask
+    as_add = np.where(keep, 0.0, -np.inf).astype(np.float32)
+    o, l = oracle.attention_ex(q, k, v, full_mask=as_add)
+    ref = F.scaled_dot_product_attention(tq, tk, tv, attn_mask=torch.from_numpy(keep))
+    assert np.max(np.abs(o - ref.numpy())) < 1e-12
+    # causal
+    o, l = oracle.attention_ex(q, k, v, causal=True)
+    ref = F.scaled_dot_product_attention(tq, tk, tv, is_causal=True)
+    assert np.max(np.abs(o - ref.numpy())) < 1e-12
+    s = (tq @ tk.transpose(-1, -2)) / np.sqrt(D)
+    s = s.masked_fill(torch.ones(Nq, Nk, dtype=torch.bool).triu(1), float("-inf"))
+    assert np.max(np.abs(l - torch.logsumexp(s, -1).numpy())) < 1e-12
+
+
+def test_ex_rows_mode_matches_full():
+    rng = _rng(24)
+    q, k, v = _randn(rng, 1, 2, 40, 8), _randn(rng, 1, 2, 33, 8), _randn(rng, 1, 2, 33, 8)
+    add = _randn(rng, 1, 2, 40, 33)
+    rows = workloads.sample_rows(40, 2, nrows=6, seed=9)
+    o, l = oracle.attention_ex(q, k, v, full_mask=add, causal=True)
+    o_r, l_r = oracle.attention_ex(q, k, v, full_mask=add, causal=True, rows=rows)
+    for bh in range(2):
+        assert np.array_equal(o_r[0, bh], o[0, bh, rows[bh]])
+        assert np.array_equal(l_r[0, bh], l[0, bh, rows[bh]])
