@@ -70,6 +70,46 @@ typedef enum {
 int fa_fwd(const void* q, const void* k, const void* v, const float* mask, void* out, float* lse,
            int B, int H, int Nq, int Nk, int D, float scale, void* stream);
 
+/* Kinds of mask fa_fwd_ex accepts. */
+typedef enum {
+    FA_MASK_NONE = 0,
+    FA_MASK_KEY_PADDING = 1, /* fp32 [B, Nk], added to every query row (as fa_fwd's mask) */
+    FA_MASK_ADDITIVE = 2,    /* fp32 [B, heads, Nq, Nk], added to each scaled score */
+    FA_MASK_BOOL = 3         /* uint8 [B, heads, Nq, Nk]: nonzero keeps the pair, 0 excludes it */
+} fa_mask_kind;
+
+/* A mask for fa_fwd_ex: `data` is a contiguous device array of the kind's
+ * layout; `heads` (ADDITIVE and BOOL) is 1 to broadcast over heads, or H. */
+typedef struct fa_mask {
+    int kind;
+    const void* data;
+    int heads;
+} fa_mask;
+
+/*
+ * fa_fwd_ex — fa_fwd with general masks and an optional causal triangle.
+ *
+ * A per-(query, key) additive mask is added after the scale, like the
+ * key-padding mask ("Step 3.7 Flash" §2.3, where ignored positions carry a
+ * large negative); a boolean mask excludes the pairs where it is 0, i.e. it
+ * is the additive mask 0 / -inf ("FlashAttention原理与工业实战" §2.1,
+ * masked_fill(mask == 0, -inf)).  causal != 0 also excludes key j > query i
+ * (top-left aligned: row i sees keys 0..i, the lower-triangular mask of that
+ * page's §4.3 causal example); key blocks entirely above the diagonal are not
+ * computed.
+ *
+ *   mask  NULL or kind FA_MASK_NONE: no mask; otherwise as fa_mask above.  An
+ *         ADDITIVE mask must be 4-byte aligned; a mask must not overlap out or lse.
+ *   other arguments as fa_fwd.
+ *
+ * Rows left with no key give O = 0, LSE = -inf.  Errors as fa_fwd, plus
+ * FA_ERR_INVALID_ARGUMENT for an unknown kind, NULL data, heads not 1 or H,
+ * or a misaligned or overlapping mask.
+ */
+int fa_fwd_ex(const void* q, const void* k, const void* v, const fa_mask* mask, int causal,
+              void* out, float* lse, int B, int H, int Nq, int Nk, int D, float scale,
+              void* stream);
+
 /*
  * fa_fwd_split — the same forward with the key axis cut into `num_splits`
  * ranges computed by separate work units, then merged.

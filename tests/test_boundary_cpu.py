@@ -109,3 +109,22 @@ def _split_call(**kw):
 ])
 def test_split_validation_before_any_cuda_call(lib, kw, code):
     assert _split_call(**kw) == code
+
+
+def test_fa_fwd_ex_mask_validation_before_any_cuda_call(lib):
+    from unet_fa_fwd_gb300.binding import FaMask
+    raw = fa.load_library()
+    a = FAKE
+    for kind, data, heads, code in [(7, 0x1000, 1, 1), (2, None, 1, 1), (2, 0x1002, 1, 1),
+                                    (3, 0x1000, 5, 1), (1, None, 1, 1)]:
+        m = FaMask(kind, data, heads)
+        rc = raw.fa_fwd_ex(a["q"], a["k"], a["v"], ctypes.byref(m), 0, a["out"], a["lse"], a["B"],
+                           a["H"], a["Nq"], a["Nk"], a["D"], ctypes.c_float(a["scale"]), None)
+        assert rc == code, (kind, data, heads)
+    # a valid call without a GPU reaches the CUDA set-up and fails there
+    import torch
+    if not torch.cuda.is_available():
+        m = FaMask(3, 0x90000, 2)
+        rc = raw.fa_fwd_ex(a["q"], a["k"], a["v"], ctypes.byref(m), 1, a["out"], a["lse"], a["B"],
+                           a["H"], a["Nq"], a["Nk"], a["D"], ctypes.c_float(a["scale"]), None)
+        assert rc == 3

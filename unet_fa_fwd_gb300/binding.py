@@ -21,8 +21,18 @@ FA_ERR_UNSUPPORTED = 2
 FA_ERR_CUDA = 3
 FA_ERR_TIMEOUT = 4
 
+FA_MASK_NONE = 0
+FA_MASK_KEY_PADDING = 1
+FA_MASK_ADDITIVE = 2
+FA_MASK_BOOL = 3
+
 _lib = None
 _lock = threading.Lock()
+
+
+class FaMask(ctypes.Structure):
+    """The C struct fa_mask."""
+    _fields_ = [("kind", ctypes.c_int), ("data", ctypes.c_void_p), ("heads", ctypes.c_int)]
 
 
 def library_path() -> str:
@@ -43,6 +53,9 @@ def load_library() -> ctypes.CDLL:
             vp, i32, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
             lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp]
             lib.fa_fwd.restype = i32
+            lib.fa_fwd_ex.argtypes = [vp, vp, vp, ctypes.POINTER(FaMask), i32, vp, vp, i32, i32, i32,
+                                      i32, i32, f32, vp]
+            lib.fa_fwd_ex.restype = i32
             sz = ctypes.c_size_t
             lib.fa_fwd_split.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32,
                                          vp, sz, vp]
@@ -126,6 +139,62 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, mask: torch.Tensor | 
     out = torch.empty((B, H, Nq, D), dtype=torch.bfloat16, device=q.device)
     lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
     fa_fwd(q, k, v, mask, out, lse, scale=scale, stream=stream)
+    return out, lse
+
+
+def fa_fwd_ex(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Tensor,
+              lse: torch.Tensor, key_mask: torch.Tensor | None = None,
+              full_mask: torch.Tensor | None = None, causal: bool = False,
+              scale: float | None = None, stream=None) -> None:
+    """Forward with general masks into caller buffers.
+
+    key_mask: fp32 [B, Nk] additive; full_mask: fp32 [B, 1|H, Nq, Nk] additive or
+    bool/uint8 [B, 1|H, Nq, Nk] (True/nonzero keeps the pair); causal: exclude key j > query i.
+    At most one of key_mask / full_mask.
+    """
+    B, H, Nq, D = q.shape
+    Nk = k.shape[2]
+    _check(q, "q", torch.bfloat16, (B, H, Nq, D))
+    _check(k, "k", torch.bfloat16, (B, H, Nk, D))
+    _check(v, "v", torch.bfloat16, (B, H, Nk, D))
+    _check(out, "out", torch.bfloat16, (B, H, Nq, D))
+    _check(lse, "lse", torch.float32, (B, H, Nq))
+    if key_mask is not None and full_mask is not None:
+        raise ValueError("pass key_mask or full_mask, not both")
+    m = FaMask(FA_MASK_NONE, None, 1)
+    if key_mask is not None:
+        _check(key_mask, "key_mask", torch.float32, (B, Nk))
+        m = FaMask(FA_MASK_KEY_PADDING, key_mask.data_ptr(), 1)
+    elif full_mask is not None:
+        if full_mask.dim() != 4 or full_mask.shape[1] not in (1, H):
+            raise ValueError("full_mask must be [B, 1|H, Nq, Nk]")
+        heads = full_mask.shape[1]
+        if full_mask.dtype == torch.float32:
+            _check(full_mask, "full_mask", torch.float32, (B, heads, Nq, Nk))
+            m = FaMask(FA_MASK_ADDITIVE, full_mask.data_ptr(), heads)
+        elif full_mask.dtype in (torch.bool, torch.uint8):
+            _check(full_mask, "full_mask", full_mask.dtype, (B, heads, Nq, Nk))
+            m = FaMask(FA_MASK_BOOL, full_mask.data_ptr(), heads)
+        else:
+            raise TypeError("full_mask must be float32 (additive) or bool/uint8")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    rc = load_library().fa_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), ctypes.byref(m),
+                                   int(bool(causal)), out.data_ptr(), lse.data_ptr(), B, H, Nq, Nk,
+                                   D, ctypes.c_float(scale), _stream_handle(stream))
+    if rc != FA_OK:
+        raise RuntimeError(f"fa_fwd_ex failed: {status_string(rc)}")
+
+
+def fwd_ex(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, key_mask: torch.Tensor | None = None,
+           full_mask: torch.Tensor | None = None, causal: bool = False,
+           scale: float | None = None, stream=None):
+    """Allocate outputs and run fa_fwd_ex; returns (O, LSE)."""
+    B, H, Nq, D = q.shape
+    out = torch.empty((B, H, Nq, D), dtype=torch.bfloat16, device=q.device)
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    fa_fwd_ex(q, k, v, out, lse, key_mask=key_mask, full_mask=full_mask, causal=causal,
+              scale=scale, stream=stream)
     return out, lse
 
 

@@ -187,6 +187,7 @@ int prepare(const void* q, const void* k, const void* v, const float* mask, void
   prm->units_per_bh = (int)upb;
   prm->nkv = (Nk + 127) / 128;
   prm->num_splits = 1;
+  prm->mask_heads = 1;
   prm->num_units = (int)(BH * upb);
   prm->scale_log2 = (float)((double)scale * 1.4426950408889634);
   prm->timeout_ns = timeout_ns_from_env();
@@ -217,6 +218,40 @@ int fa_fwd(const void* q, const void* k, const void* v, const float* mask, void*
   DeviceState* st = nullptr;
   const int rc = prepare(q, k, v, mask, out, lse, B, H, Nq, Nk, D, scale, &prm, &st);
   if (rc != FA_OK) return rc;
+  return launch_fwd(prm, *st, D, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int fa_fwd_ex(const void* q, const void* k, const void* v, const fa_mask* mask, int causal,
+              void* out, float* lse, int B, int H, int Nq, int Nk, int D, float scale,
+              void* stream) {
+  const int kind = mask ? mask->kind : FA_MASK_NONE;
+  if (kind != FA_MASK_NONE && kind != FA_MASK_KEY_PADDING && kind != FA_MASK_ADDITIVE &&
+      kind != FA_MASK_BOOL)
+    return FA_ERR_INVALID_ARGUMENT;
+  if (kind != FA_MASK_NONE && !mask->data) return FA_ERR_INVALID_ARGUMENT;
+  const bool full = kind == FA_MASK_ADDITIVE || kind == FA_MASK_BOOL;
+  if (full) {
+    if (mask->heads != 1 && mask->heads != H) return FA_ERR_INVALID_ARGUMENT;
+    if (kind == FA_MASK_ADDITIVE && (reinterpret_cast<uintptr_t>(mask->data) & 3u))
+      return FA_ERR_INVALID_ARGUMENT;
+  }
+  const float* key_mask = kind == FA_MASK_KEY_PADDING ? static_cast<const float*>(mask->data) : nullptr;
+  fa::Params prm;
+  DeviceState* st = nullptr;
+  int rc = prepare(q, k, v, key_mask, out, lse, B, H, Nq, Nk, D, scale, &prm, &st);
+  if (rc != FA_OK) return rc;
+  if (full) {
+    const size_t fm_bytes =
+        (size_t)B * mask->heads * Nq * Nk * (kind == FA_MASK_ADDITIVE ? sizeof(float) : 1);
+    const size_t rows = (size_t)B * H * Nq;
+    if (ranges_overlap(mask->data, fm_bytes, out, rows * D * 2) ||
+        ranges_overlap(mask->data, fm_bytes, lse, rows * 4))
+      return FA_ERR_INVALID_ARGUMENT;
+    prm.full_mask = mask->data;
+    prm.full_mask_bool = kind == FA_MASK_BOOL;
+    prm.mask_heads = mask->heads;
+  }
+  prm.causal = causal ? 1 : 0;
   return launch_fwd(prm, *st, D, reinterpret_cast<cudaStream_t>(stream));
 }
 

@@ -72,8 +72,8 @@ struct Cfg {
   // REGS_OTHER; the sum stays within 384*168, so the increase never waits on
   // registers that do not exist.
 #ifndef FA_REGS_SOFTMAX
-#define FA_REGS_SOFTMAX 192
-#define FA_REGS_OTHER 120
+#define FA_REGS_SOFTMAX 184
+#define FA_REGS_OTHER 136
 #endif
   static constexpr int REGS_SOFTMAX = FA_REGS_SOFTMAX;
   static constexpr int REGS_OTHER = FA_REGS_OTHER;
@@ -86,7 +86,11 @@ struct Params {  // 64-byte aligned through its CUtensorMap members
   CUtensorMap tm_v;  // [BH][Nk][D]
   __nv_bfloat16* out;  // [BH][Nq][D]
   float* lse;          // [BH][Nq]
-  const float* mask;   // [B][Nk] or nullptr
+  const float* mask;   // key padding [B][Nk] or nullptr
+  const void* full_mask;  // per (query, key) mask [B][mask_heads][Nq][Nk] or nullptr
+  int full_mask_bool;     // 0: additive fp32; 1: uint8, nonzero = keep, 0 = -inf
+  int mask_heads;         // 1 (broadcast over heads) or H
+  int causal;             // exclude key j > query i
   int H, Nq, Nk, BH;
   int num_units;       // BH * units_per_bh * num_splits
   int units_per_bh;    // ceil(ceil(Nq/128)/2)
@@ -114,6 +118,12 @@ __device__ __forceinline__ Unit decode_unit(const Params& p, int u) {
   // Balanced ranges: range s covers key blocks [s*nkv/S, (s+1)*nkv/S).
   r.tile0 = (int)((long long)r.split * p.nkv / p.num_splits);
   r.ntiles = (int)((long long)(r.split + 1) * p.nkv / p.num_splits) - r.tile0;
+  if (p.causal) {
+    // Key blocks past the unit's last query row are fully masked: skip them
+    // (causal launches use one key range, so at least one block remains).
+    const int last_row = min(r.q0 + 255, p.Nq - 1);
+    r.ntiles = min(r.ntiles, last_row / 128 + 1 - r.tile0);
+  }
   return r;
 }
 
@@ -469,6 +479,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       if (t == 1 && !(q0 + 128 < p.Nq)) continue;
       const int qrow = q0 + t * 128 + row;
       const float* mask_b = p.mask ? p.mask + (size_t)(bh / p.H) * p.Nk : nullptr;
+      const bool any_full_mask = p.full_mask != nullptr;  // warp-uniform
+      const int tile_row0 = q0 + t * 128;                 // first query row of this tile
       float m = -INFINITY;  // running max of t_ij (log2 domain)
       float l = 0.f;        // running denominator relative to m
 
@@ -488,7 +500,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         // Fast path: full key block, no mask, non-negative scale — the row max
         // is taken on raw scores and scaled once.  Otherwise scores are
         // materialised in the log2 domain with the mask and the Nk tail.
-        const bool general = (mask_b != nullptr) || (kbase + 128 > p.Nk) || !(scale_log2 >= 0.f);
+        const bool general = (mask_b != nullptr) || any_full_mask || (kbase + 128 > p.Nk) ||
+                             !(scale_log2 >= 0.f) || (p.causal && kbase + 127 > tile_row0);
         float mx;
         if (!general) {
           float a0 = s[0], a1 = s[1], a2 = s[2], a3 = s[3];
@@ -502,13 +515,27 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
           mx = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)) * scale_log2;
         } else {
           mx = -INFINITY;
+          // This row of the per-(query, key) mask (rows past Nq read nothing).
+          const float* fmask_f = nullptr;
+          const uint8_t* fmask_b = nullptr;
+          if (any_full_mask && qrow < p.Nq) {
+            const size_t fm_row =
+                ((size_t)(bh / p.H) * p.mask_heads + (p.mask_heads == 1 ? 0 : bh % p.H)) * p.Nq +
+                (size_t)qrow;
+            if (p.full_mask_bool)
+              fmask_b = static_cast<const uint8_t*>(p.full_mask) + fm_row * p.Nk;
+            else
+              fmask_f = static_cast<const float*>(p.full_mask) + fm_row * p.Nk;
+          }
 #pragma unroll
           for (int c = 0; c < 128; ++c) {
             const int key = kbase + c;
             float tv = -INFINITY;
-            if (key < p.Nk) {
+            if (key < p.Nk && !(p.causal && key > qrow)) {
               tv = s[c] * scale_log2;
               if (mask_b) tv = fmaf(__ldg(mask_b + key), kLog2e, tv);
+              if (fmask_f) tv = fmaf(__ldg(fmask_f + key), kLog2e, tv);
+              if (fmask_b && __ldg(fmask_b + key) == 0) tv = -INFINITY;
             }
             s[c] = tv;
             mx = fmaxf(mx, tv);
