@@ -43,6 +43,9 @@ def _load():
         lib.fa_oracle_fwd_ex.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, vp, i32, dp, dp, i32,
                                          i32, i32, i32, i32, f64, i32]
         lib.fa_oracle_fwd_ex.restype = i32
+        lib.fa_oracle_window.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, dp, dp, i32,
+                                         i32, i32, f64, i32]
+        lib.fa_oracle_window.restype = i32
         lib.fa_oracle_probs.argtypes = [vp, vp, vp, i32, i32, i32, i32, dp, i32, i32, i32, i32, i32, f64]
         lib.fa_oracle_probs.restype = i32
         _lib = lib
@@ -159,6 +162,35 @@ def attention_ex(q: np.ndarray, k: np.ndarray, v: np.ndarray, mask: np.ndarray |
                               out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
                               lse.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
                               B, H, Nq, Nk, D, float(scale), int(nthreads or default_threads()))
+    if rc != 0:
+        raise RuntimeError(f"oracle failed with code {rc}")
+    return out, lse
+
+
+def window_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, img_h: int, img_w: int,
+                     win_h: int, win_w: int, shift_h: int = 0, shift_w: int = 0,
+                     scale: float | None = None, nthreads: int | None = None):
+    """fp64 window / shifted-window attention on an img_h x img_w token grid.
+
+    q, k, v: [B, H, img_h*img_w, D] in row-major token order.  Returns (O, LSE)
+    in the same order.
+    """
+    lib = _load()
+    B, H, N, D = q.shape
+    if N != img_h * img_w or k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must be [B, H, img_h*img_w, D]")
+    qa, dt = _as_input(q)
+    ka, _ = _as_input(k)
+    va, _ = _as_input(v)
+    if scale is None:
+        scale = 1.0 / np.sqrt(D)
+    out = np.empty((B, H, N, D), dtype=np.float64)
+    lse = np.empty((B, H, N), dtype=np.float64)
+    rc = lib.fa_oracle_window(_ptr(qa), _ptr(ka), _ptr(va), dt, img_h, img_w, win_h, win_w,
+                              shift_h, shift_w,
+                              out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
+                              lse.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
+                              B, H, D, float(scale), int(nthreads or default_threads()))
     if rc != 0:
         raise RuntimeError(f"oracle failed with code {rc}")
     return out, lse

@@ -75,6 +75,8 @@ typedef struct {
     const float* full_mask; /* [B, mask_heads, Nq, Nk] additive, or NULL */
     int mask_heads;         /* 1 (broadcast over heads) or H */
     int causal;             /* key j > query i is excluded */
+    int win;                /* window attention: tokens are an img_h x img_w grid */
+    int img_h, img_w, win_h, win_w, shift_h, shift_w;
     int dtype;
     int B, H, Nq, Nk, D;
     double scale;
@@ -85,6 +87,16 @@ typedef struct {
     int64_t total_items;          /* number of (head, row) items */
     int64_t next_item;            /* shared work counter */
 } oracle_job;
+
+/* Window of token t (row-major on the img_h x img_w grid) after the grid is
+ * rolled by (-shift_h, -shift_w), as a cyclic shift moves the token at (r, c)
+ * to (r - shift_h, c - shift_w); windows are win_h x win_w tiles of that grid. */
+static int64_t window_of(const oracle_job* job, int64_t t) {
+    const int64_t r = t / job->img_w, c = t % job->img_w;
+    const int64_t rs = ((r - job->shift_h) % job->img_h + job->img_h) % job->img_h;
+    const int64_t cs = ((c - job->shift_w) % job->img_w + job->img_w) % job->img_w;
+    return (rs / job->win_h) * (job->img_w / job->win_w) + cs / job->win_w;
+}
 
 /* One query row of one head: materialise the score row, then softmax, then the
  * weighted sum of V rows.  s and p are scratch buffers of length Nk. */
@@ -109,6 +121,7 @@ static void attend_one_row(const oracle_job* job, int64_t bh, int64_t i, double*
             sij += (double)job->full_mask[((b * job->mask_heads + hm) * Nq + i) * Nk + j];
         }
         if (job->causal && j > i) sij = -INFINITY;
+        if (job->win && window_of(job, j) != window_of(job, i)) sij = -INFINITY;
         s[j] = sij;
     }
 
@@ -199,8 +212,8 @@ int fa_oracle_fwd(const void* q, const void* k, const void* v, const float* mask
                   int nthreads) {
     if (!q || !k || !v || !out || !lse || check_shape(B, H, Nq, Nk, D)) return 1;
     if (dtype != ORACLE_DTYPE_F32 && dtype != ORACLE_DTYPE_BF16) return 1;
-    oracle_job job = {q, k, v, mask, NULL, 1, 0, dtype, B, H, Nq, Nk, D, scale, NULL, 0, out, lse,
-                      (int64_t)B * H * Nq, 0};
+    oracle_job job = {q, k, v, mask, NULL, 1, 0, 0, 0, 0, 0, 0, 0, 0, dtype, B, H, Nq, Nk, D, scale,
+                      NULL, 0, out, lse, (int64_t)B * H * Nq, 0};
     return run_job(&job, nthreads);
 }
 
@@ -222,8 +235,8 @@ int fa_oracle_fwd_ex(const void* q, const void* k, const void* v, const float* m
             if (rows[t] < 0 || rows[t] >= Nq) return 1;
     }
     oracle_job job = {q, k, v, mask, full_mask, mask_heads < 1 ? 1 : mask_heads, causal ? 1 : 0,
-                      dtype, B, H, Nq, Nk, D, scale, rows, rows ? nrows : 0, out, lse,
-                      (int64_t)B * H * (rows ? nrows : Nq), 0};
+                      0, 0, 0, 0, 0, 0, 0, dtype, B, H, Nq, Nk, D, scale, rows, rows ? nrows : 0,
+                      out, lse, (int64_t)B * H * (rows ? nrows : Nq), 0};
     return run_job(&job, nthreads);
 }
 
@@ -237,8 +250,28 @@ int fa_oracle_rows(const void* q, const void* k, const void* v, const float* mas
     if (dtype != ORACLE_DTYPE_F32 && dtype != ORACLE_DTYPE_BF16) return 1;
     for (int64_t t = 0; t < (int64_t)B * H * nrows; ++t)
         if (rows[t] < 0 || rows[t] >= Nq) return 1;
-    oracle_job job = {q, k, v, mask, NULL, 1, 0, dtype, B, H, Nq, Nk, D, scale, rows, nrows, out,
-                      lse, (int64_t)B * H * nrows, 0};
+    oracle_job job = {q, k, v, mask, NULL, 1, 0, 0, 0, 0, 0, 0, 0, 0, dtype, B, H, Nq, Nk, D, scale,
+                      rows, nrows, out, lse, (int64_t)B * H * nrows, 0};
+    return run_job(&job, nthreads);
+}
+
+/* Window attention on an img_h x img_w token grid (N = img_h * img_w tokens,
+ * q, k, v [B, H, N, D] in row-major token order): the grid is cyclically
+ * shifted by (-shift_h, -shift_w), cut into win_h x win_w windows, and each
+ * token attends only to the tokens of its own window (the "Step 3.7 Flash"
+ * §2.1 / §3.2 window and shifted-window attention, read as a cyclic shift
+ * with no further mask).  O [B, H, N, D], LSE [B, H, N] in the original
+ * token order.  img_h % win_h == 0 and img_w % win_w == 0 are required. */
+int fa_oracle_window(const void* q, const void* k, const void* v, int dtype, int img_h, int img_w,
+                     int win_h, int win_w, int shift_h, int shift_w, double* out, double* lse,
+                     int B, int H, int D, double scale, int nthreads) {
+    if (img_h < 1 || img_w < 1 || win_h < 1 || win_w < 1) return 1;
+    if (img_h % win_h || img_w % win_w) return 1;
+    const int N = img_h * img_w;
+    if (!q || !k || !v || !out || !lse || check_shape(B, H, N, N, D)) return 1;
+    if (dtype != ORACLE_DTYPE_F32 && dtype != ORACLE_DTYPE_BF16) return 1;
+    oracle_job job = {q, k, v, NULL, NULL, 1, 0, 1, img_h, img_w, win_h, win_w, shift_h, shift_w,
+                      dtype, B, H, N, N, D, scale, NULL, 0, out, lse, (int64_t)B * H * N, 0};
     return run_job(&job, nthreads);
 }
 

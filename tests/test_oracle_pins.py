@@ -435,3 +435,61 @@ def test_ex_rows_mode_matches_full():
     for bh in range(2):
         assert np.array_equal(o_r[0, bh], o[0, bh, rows[bh]])
         assert np.array_equal(l_r[0, bh], l[0, bh, rows[bh]])
+
+
+# ---------------------------------------------------------------------------
+# Window / shifted-window attention (the oracle's fa_oracle_window).
+# ---------------------------------------------------------------------------
+
+def _grid_inputs(seed, B=1, H=2, img=(8, 12), D=8):
+    rng = _rng(seed)
+    N = img[0] * img[1]
+    return [_randn(rng, B, H, N, D) for _ in range(3)]
+
+
+def test_window_equal_to_image_is_full_attention():
+    q, k, v = _grid_inputs(30)
+    o, l = oracle.window_attention(q, k, v, 8, 12, 8, 12, shift_h=3, shift_w=5)
+    o_f, l_f = oracle.attention(q, k, v)
+    assert np.max(np.abs(o - o_f)) < 1e-12 and np.max(np.abs(l - l_f)) < 1e-12
+
+
+def test_one_by_one_windows_attend_to_self():
+    q, k, v = _grid_inputs(31)
+    o, l = oracle.window_attention(q, k, v, 8, 12, 1, 1, scale=0.5)
+    assert np.array_equal(o, v.astype(np.float64))
+    s_ii = 0.5 * np.einsum("bhnd,bhnd->bhn", q.astype(np.float64), k.astype(np.float64))
+    assert np.max(np.abs(l - s_ii)) < 1e-12
+
+
+def test_unshifted_windows_are_independent_attention_problems():
+    """Each 4x6 window, gathered into its own tensor, is plain attention."""
+    q, k, v = _grid_inputs(32)
+    o, l = oracle.window_attention(q, k, v, 8, 12, 4, 6)
+    grid = np.arange(96).reshape(8, 12)
+    for wr in range(2):
+        for wc in range(2):
+            idx = grid[wr * 4:(wr + 1) * 4, wc * 6:(wc + 1) * 6].reshape(-1)
+            o_w, l_w = oracle.attention(q[:, :, idx].copy(), k[:, :, idx].copy(), v[:, :, idx].copy())
+            assert np.max(np.abs(o[:, :, idx] - o_w)) < 1e-12
+            assert np.max(np.abs(l[:, :, idx] - l_w)) < 1e-12
+
+
+def test_shift_is_a_cyclic_roll_of_the_grid():
+    """Shifted windows = roll the grid by (-sh, -sw), unshifted windows, roll back."""
+    q, k, v = _grid_inputs(33)
+    sh, sw = 2, 3
+    o, l = oracle.window_attention(q, k, v, 8, 12, 4, 6, shift_h=sh, shift_w=sw)
+
+    def roll(x, a, b):
+        B, H, N, D = x.shape
+        return np.roll(x.reshape(B, H, 8, 12, D), (a, b), axis=(2, 3)).reshape(B, H, N, D)
+
+    o_r, l_r = oracle.window_attention(roll(q, -sh, -sw), roll(k, -sh, -sw), roll(v, -sh, -sw),
+                                       8, 12, 4, 6)
+    assert np.max(np.abs(o - roll(o_r, sh, sw))) < 1e-12
+    assert np.max(np.abs(l - roll(l_r[..., None], sh, sw)[..., 0])) < 1e-12
+    # a shift by whole windows regroups the same windows: same result
+    o2, _ = oracle.window_attention(q, k, v, 8, 12, 4, 6, shift_h=4, shift_w=6)
+    o0, _ = oracle.window_attention(q, k, v, 8, 12, 4, 6)
+    assert np.max(np.abs(o2 - o0)) < 1e-12
