@@ -128,3 +128,20 @@ def test_fa_fwd_ex_mask_validation_before_any_cuda_call(lib):
         rc = raw.fa_fwd_ex(a["q"], a["k"], a["v"], ctypes.byref(m), 1, a["out"], a["lse"], a["B"],
                            a["H"], a["Nq"], a["Nk"], a["D"], ctypes.c_float(a["scale"]), None)
         assert rc == 3
+
+
+def test_window_validation_before_any_cuda_call(lib):
+    raw = fa.load_library()
+    assert fa.window_workspace_bytes(1, 2, 8, 8, 64) == 4 * 8192 + 512
+    assert fa.window_workspace_bytes(0, 2, 8, 8, 64) == 0
+
+    def call(img=(8, 8), win=(4, 4), D=64, ws=0xA0000, ws_bytes=1 << 20, q=0x10000):
+        return raw.fa_fwd_window(q, 0x20000, 0x30000, 0x40000, 0x50000, 1, 2, img[0], img[1], D,
+                                 win[0], win[1], 1, 1, ctypes.c_float(0.1), ws, ws_bytes, None)
+    assert call(win=(3, 4)) == 1       # windows must tile the grid
+    assert call(win=(0, 4)) == 1
+    assert call(D=48) == 2
+    assert call(ws=None) == 1
+    assert call(ws=0xA0008) == 1       # misaligned workspace
+    assert call(ws_bytes=100) == 1
+    assert call(q=None) == 1

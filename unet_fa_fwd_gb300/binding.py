@@ -57,6 +57,11 @@ def load_library() -> ctypes.CDLL:
                                       i32, i32, f32, vp]
             lib.fa_fwd_ex.restype = i32
             sz = ctypes.c_size_t
+            lib.fa_fwd_window.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32,
+                                          i32, f32, vp, sz, vp]
+            lib.fa_fwd_window.restype = i32
+            lib.fa_window_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
+            lib.fa_window_workspace_bytes.restype = sz
             lib.fa_fwd_split.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32,
                                          vp, sz, vp]
             lib.fa_fwd_split.restype = i32
@@ -195,6 +200,33 @@ def fwd_ex(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, key_mask: torch.Te
     lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
     fa_fwd_ex(q, k, v, out, lse, key_mask=key_mask, full_mask=full_mask, causal=causal,
               scale=scale, stream=stream)
+    return out, lse
+
+
+def window_workspace_bytes(B: int, H: int, img_h: int, img_w: int, D: int) -> int:
+    return int(load_library().fa_window_workspace_bytes(B, H, img_h, img_w, D))
+
+
+def fwd_window(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, img_h: int, img_w: int,
+               win_h: int, win_w: int, shift_h: int = 0, shift_w: int = 0,
+               scale: float | None = None, stream=None):
+    """Window / shifted-window attention; q, k, v bf16 [B, H, img_h*img_w, D] in grid order.
+    Allocates outputs and the workspace with torch; returns (O, LSE)."""
+    B, H, N, D = q.shape
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check(t, n, torch.bfloat16, (B, H, N, D))
+    out = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    ws = torch.empty(max(16, window_workspace_bytes(B, H, img_h, img_w, D)), dtype=torch.uint8,
+                     device=q.device)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    rc = load_library().fa_fwd_window(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                       lse.data_ptr(), B, H, img_h, img_w, D, win_h, win_w,
+                                       shift_h, shift_w, ctypes.c_float(scale), ws.data_ptr(),
+                                       ws.numel(), _stream_handle(stream))
+    if rc != FA_OK:
+        raise RuntimeError(f"fa_fwd_window failed: {status_string(rc)}")
     return out, lse
 
 

@@ -19,6 +19,7 @@
 
 #include "fa.h"
 #include "fa_fwd_kernel.cuh"
+#include "fa_window.cuh"
 
 namespace {
 
@@ -351,6 +352,66 @@ int fa_fwd_split_noalloc(const void* q, const void* k, const void* v, const floa
   // nothing in the scratch needs clearing between calls.
   return fa_fwd_split(q, k, v, mask, out, lse, B, H, Nq, Nk, D, scale, splits, scratch,
                       (size_t)FA_NOALLOC_SCRATCH_BYTES, stream);
+}
+
+size_t fa_window_workspace_bytes(int B, int H, int img_h, int img_w, int D) {
+  if (B < 1 || H < 1 || img_h < 1 || img_w < 1 || D < 1) return 0;
+  const size_t rows = (size_t)B * H * img_h * img_w;
+  return 4 * align256(rows * D * 2) + align256(rows * 4);
+}
+
+int fa_fwd_window(const void* q, const void* k, const void* v, void* out, float* lse, int B, int H,
+                  int img_h, int img_w, int D, int win_h, int win_w, int shift_h, int shift_w,
+                  float scale, void* workspace, size_t workspace_bytes, void* stream) {
+  // ---- validation: no CUDA call before this block passes ----
+  if (!q || !k || !v || !out || !lse || !workspace) return FA_ERR_INVALID_ARGUMENT;
+  if (B < 1 || H < 1 || img_h < 1 || img_w < 1 || win_h < 1 || win_w < 1)
+    return FA_ERR_INVALID_ARGUMENT;
+  if (img_h % win_h || img_w % win_w) return FA_ERR_INVALID_ARGUMENT;
+  if (D != 32 && D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+  if ((int64_t)img_h * img_w > INT_MAX) return FA_ERR_INVALID_ARGUMENT;
+  if (!aligned16(workspace) || workspace_bytes < fa_window_workspace_bytes(B, H, img_h, img_w, D))
+    return FA_ERR_INVALID_ARGUMENT;
+  const int N = img_h * img_w;
+  const size_t rows = (size_t)B * H * N;
+  const size_t t_bytes = rows * D * 2;
+  const size_t ws_used = fa_window_workspace_bytes(B, H, img_h, img_w, D);
+  if (ranges_overlap(workspace, ws_used, q, t_bytes) || ranges_overlap(workspace, ws_used, k, t_bytes) ||
+      ranges_overlap(workspace, ws_used, v, t_bytes) || ranges_overlap(workspace, ws_used, out, t_bytes) ||
+      ranges_overlap(workspace, ws_used, lse, rows * 4))
+    return FA_ERR_INVALID_ARGUMENT;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse))
+    return FA_ERR_INVALID_ARGUMENT;
+  fa::WindowGeom g{B, H, img_h, img_w, win_h, win_w, 0, 0, D};
+  g.shift_h = ((shift_h % img_h) + img_h) % img_h;
+  g.shift_w = ((shift_w % img_w) + img_w) % img_w;
+  const long long nw = g.windows();
+  if ((long long)B * nw > INT_MAX) return FA_ERR_INVALID_ARGUMENT;
+
+  char* ws = static_cast<char*>(workspace);
+  const size_t t_al = align256(t_bytes);
+  void* qw = ws;
+  void* kw = ws + t_al;
+  void* vw = ws + 2 * t_al;
+  void* ow = ws + 3 * t_al;
+  float* lw = reinterpret_cast<float*>(ws + 4 * t_al);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+  const long long chunks = (long long)rows * (D / 8);
+  const long long blocks = (chunks + 255) / 256;
+  if (blocks > INT_MAX) return FA_ERR_INVALID_ARGUMENT;
+  if (std::getenv("FA_FAULT_INJECT") && std::strcmp(std::getenv("FA_FAULT_INJECT"), "launch") == 0)
+    return FA_ERR_CUDA;
+  fa::fa_window_gather_kernel<<<(int)blocks, 256, 0, s>>>(
+      static_cast<const uint4*>(q), static_cast<const uint4*>(k), static_cast<const uint4*>(v),
+      static_cast<uint4*>(qw), static_cast<uint4*>(kw), static_cast<uint4*>(vw), g, chunks);
+  if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+  const int Nw = g.win_tokens();
+  int rc = fa_fwd(qw, kw, vw, nullptr, ow, lw, (int)(B * nw), H, Nw, Nw, D, scale, stream);
+  if (rc != FA_OK) return rc;
+  fa::fa_window_scatter_kernel<<<(int)blocks, 256, 0, s>>>(
+      static_cast<const uint4*>(ow), lw, static_cast<uint4*>(out), lse, g, chunks);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 int fa_read_device_status(void* stream, int* status) {
