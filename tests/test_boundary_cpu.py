@@ -132,7 +132,7 @@ def test_fa_fwd_ex_mask_validation_before_any_cuda_call(lib):
 
 def test_window_validation_before_any_cuda_call(lib):
     raw = fa.load_library()
-    assert fa.window_workspace_bytes(1, 2, 8, 8, 64) == 4 * 8192 + 512
+    assert fa.window_workspace_bytes(1, 2, 8, 8, 64) == 4 * (2 * 64 * 64 * 2) + 2 * 64 * 4
     assert fa.window_workspace_bytes(0, 2, 8, 8, 64) == 0
 
     def call(img=(8, 8), win=(4, 4), D=64, ws=0xA0000, ws_bytes=1 << 20, q=0x10000):
