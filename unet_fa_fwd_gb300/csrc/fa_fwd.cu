@@ -165,8 +165,8 @@ int prepare(const void* q, const void* k, const void* v, const float* mask, void
     return FA_ERR_INVALID_ARGUMENT;
 
   // ---- set-up ----
-  if (std::getenv("FA_FAULT_INJECT") && std::strcmp(std::getenv("FA_FAULT_INJECT"), "launch") == 0)
-    return FA_ERR_CUDA;
+  const char* inject = std::getenv("FA_FAULT_INJECT");
+  if (inject && std::strcmp(inject, "launch") == 0) return FA_ERR_CUDA;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
   int rc = device_setup(dev, st);
@@ -192,6 +192,7 @@ int prepare(const void* q, const void* k, const void* v, const float* mask, void
   prm->num_units = (int)(BH * upb);
   prm->scale_log2 = (float)((double)scale * 1.4426950408889634);
   prm->timeout_ns = timeout_ns_from_env();
+  prm->inject_stall = (inject && std::strcmp(inject, "stall") == 0) ? 1 : 0;
   return FA_OK;
 }
 

@@ -100,6 +100,7 @@ struct Params {  // 64-byte aligned through its CUtensorMap members
   float* part_lse;     // split mode: fp32 [num_splits][BH][Nq] partial LSE
   float scale_log2;    // scale * log2(e)
   unsigned long long timeout_ns;
+  int inject_stall;    // test hook: CTA 0's producer withholds its 4th K/V tile
 };
 
 // One work unit: 256 query rows of one (b, h) against one range of key blocks.
@@ -299,6 +300,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
             ok = bounded_wait(ptx::smem_u32(&bars->kv_empty[s]), ph ^ 1, bars, p.timeout_ns);
             if (!ok) break;
             const uint32_t fb = ptx::smem_u32(&bars->kv_full[s]);
+            if (p.inject_stall && blockIdx.x == 0 && it == 3) continue;  // nothing arrives: consumers time out
             ptx::mbar_arrive_expect_tx(fb, C::TILE_BYTES);
             const void* tm = kv == 0 ? (const void*)&p.tm_k : (const void*)&p.tm_v;
             for (int c = 0; c < C::NCHUNK; ++c)
