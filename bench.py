@@ -304,6 +304,27 @@ def bench_native(args, world, rank, local):
                                 "steps": n_h}
         del hw, hoAll, hl
 
+    # ---- FP8 (e4m3 Q K^T) forward on the same workload, pre-pass included ----
+    if args.also and rank == 0:
+        ws8 = torch.empty(fa.fp8_workspace_bytes(B, H, Nq, Nk, D), dtype=torch.uint8, device=device)
+        call8 = lambda: fa.fa_fwd_fp8(q, k, v, mask, out, lse, ws8, scale=inp["scale"], stream=stream)
+        for _ in range(3):
+            call8()
+        torch.cuda.synchronize(device)
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n8 = max(5, args.steps // 10)
+        f0.record(stream)
+        for _ in range(n8):
+            call8()
+        f1.record(stream)
+        torch.cuda.synchronize(device)
+        ms8 = f0.elapsed_time(f1) / n8
+        also["fp8_qk"] = {"workload": args.workload, "ms_per_step": round(ms8, 4),
+                          "tflops": round(flops / ms8 / 1e9, 1), "steps": n8,
+                          "note": "e4m3 Q K^T with K mean smoothing, bf16 P V; "
+                                  "bf16-equivalent attention FLOPs; quantisation pre-pass timed"}
+        del ws8
+
     # ---- split-key forward on a low-occupancy shape (2 units for all SMs) ----
     if args.also and rank == 0:
         sw = workloads.make_inputs("hunyuan_720p", device=device, B=1, H=2, Nq=256, Nk=119056)

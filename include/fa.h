@@ -111,6 +111,37 @@ int fa_fwd_ex(const void* q, const void* k, const void* v, const fa_mask* mask, 
               void* stream);
 
 /*
+ * fa_fwd_fp8 — the forward with Q K^T in FP8 (e4m3), SageAttention-style
+ * ("算子加速：注意力、编译与融合", section "SageAttention": smooth K by
+ * subtracting its mean, quantise, run the low-precision product; P and V stay
+ * 16-bit, as in its first version).
+ *
+ * A pre-pass subtracts from K its per-channel mean over the keys of each head
+ * (this moves every score of row i by the same q_i . mean, so the softmax is
+ * unchanged and LSE is corrected by scale * q_i . mean), then quantises Q and
+ * the smoothed K to e4m3 with one scale per 128-row block (block max / 448).
+ * S = Q K^T runs on the tensor cores as kind::f8f6f4 (twice the bf16 rate,
+ * half the MMA instructions); the block scales are folded into the softmax's
+ * exp2 multiplier; P (bf16) V (bf16) is unchanged.  Results are close to, not
+ * equal to, the bf16 forward: the error budget is looser (see the tests).
+ *
+ *   arguments as fa_fwd (mask: fp32 key padding [B, Nk] or NULL), plus
+ *   workspace  device scratch, 16-byte aligned, at least
+ *              fa_fp8_workspace_bytes(B, H, Nq, Nk, D) bytes, owned by the caller
+ *              and not shared with a concurrent call.
+ *
+ * Five kernels are enqueued on `stream` (column sums, mean, quantise K,
+ * quantise Q, attention).  Errors as fa_fwd, plus FA_ERR_INVALID_ARGUMENT for
+ * a missing, misaligned, small or overlapping workspace.
+ */
+int fa_fwd_fp8(const void* q, const void* k, const void* v, const float* mask, void* out,
+               float* lse, int B, int H, int Nq, int Nk, int D, float scale, void* workspace,
+               size_t workspace_bytes, void* stream);
+
+/* Workspace bytes fa_fwd_fp8 needs (0 for invalid sizes). */
+size_t fa_fp8_workspace_bytes(int B, int H, int Nq, int Nk, int D);
+
+/*
  * fa_fwd_split — the same forward with the key axis cut into `num_splits`
  * ranges computed by separate work units, then merged.
  *

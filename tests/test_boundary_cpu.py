@@ -145,3 +145,18 @@ def test_window_validation_before_any_cuda_call(lib):
     assert call(ws=0xA0008) == 1       # misaligned workspace
     assert call(ws_bytes=100) == 1
     assert call(q=None) == 1
+
+
+def test_fp8_validation_before_any_cuda_call(lib):
+    raw = fa.load_library()
+    need = fa.fp8_workspace_bytes(1, 2, 100, 100, 64)
+    assert need > 2 * 100 * 64 * 2 and fa.fp8_workspace_bytes(1, 2, 100, 100, 48) == 0
+
+    def call(ws=0xA0000, ws_bytes=1 << 24, D=64, q=0x10000):
+        return raw.fa_fwd_fp8(q, 0x20000, 0x30000, None, 0x40000, 0x50000, 1, 2, 100, 100, D,
+                              ctypes.c_float(0.1), ws, ws_bytes, None)
+    assert call(ws=None) == 1
+    assert call(ws=0xA0008) == 1
+    assert call(ws_bytes=need - 1) == 1
+    assert call(D=48) == 2
+    assert call(q=None) == 1

@@ -60,6 +60,10 @@ def load_library() -> ctypes.CDLL:
             lib.fa_fwd_window.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32,
                                           i32, f32, vp, sz, vp]
             lib.fa_fwd_window.restype = i32
+            lib.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp, sz, vp]
+            lib.fa_fwd_fp8.restype = i32
+            lib.fa_fp8_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
+            lib.fa_fp8_workspace_bytes.restype = sz
             lib.fa_window_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
             lib.fa_window_workspace_bytes.restype = sz
             lib.fa_fwd_split.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32,
@@ -200,6 +204,49 @@ def fwd_ex(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, key_mask: torch.Te
     lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
     fa_fwd_ex(q, k, v, out, lse, key_mask=key_mask, full_mask=full_mask, causal=causal,
               scale=scale, stream=stream)
+    return out, lse
+
+
+def fp8_workspace_bytes(B: int, H: int, Nq: int, Nk: int, D: int) -> int:
+    return int(load_library().fa_fp8_workspace_bytes(B, H, Nq, Nk, D))
+
+
+def fa_fwd_fp8(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, mask: torch.Tensor | None,
+               out: torch.Tensor, lse: torch.Tensor, workspace: torch.Tensor,
+               scale: float | None = None, stream=None) -> None:
+    """FP8 (e4m3) Q K^T forward into caller buffers; `workspace` holds at least
+    fp8_workspace_bytes(...) bytes."""
+    B, H, Nq, D = q.shape
+    Nk = k.shape[2]
+    _check(q, "q", torch.bfloat16, (B, H, Nq, D))
+    _check(k, "k", torch.bfloat16, (B, H, Nk, D))
+    _check(v, "v", torch.bfloat16, (B, H, Nk, D))
+    _check(out, "out", torch.bfloat16, (B, H, Nq, D))
+    _check(lse, "lse", torch.float32, (B, H, Nq))
+    if mask is not None:
+        _check(mask, "mask", torch.float32, (B, Nk))
+    if not workspace.is_cuda or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    rc = load_library().fa_fwd_fp8(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                    None if mask is None else mask.data_ptr(), out.data_ptr(),
+                                    lse.data_ptr(), B, H, Nq, Nk, D, ctypes.c_float(scale),
+                                    workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                    _stream_handle(stream))
+    if rc != FA_OK:
+        raise RuntimeError(f"fa_fwd_fp8 failed: {status_string(rc)}")
+
+
+def fwd_fp8(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, mask: torch.Tensor | None = None,
+            scale: float | None = None, stream=None):
+    """Allocate outputs and workspace (torch) and run the FP8 Q K^T forward."""
+    B, H, Nq, D = q.shape
+    Nk = k.shape[2]
+    out = torch.empty((B, H, Nq, D), dtype=torch.bfloat16, device=q.device)
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    ws = torch.empty(fp8_workspace_bytes(B, H, Nq, Nk, D), dtype=torch.uint8, device=q.device)
+    fa_fwd_fp8(q, k, v, mask, out, lse, ws, scale=scale, stream=stream)
     return out, lse
 
 

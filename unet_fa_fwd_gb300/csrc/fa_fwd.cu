@@ -19,6 +19,7 @@
 
 #include "fa.h"
 #include "fa_fwd_kernel.cuh"
+#include "fa_quant.cuh"
 #include "fa_window.cuh"
 
 namespace {
@@ -29,7 +30,7 @@ struct DeviceState {
   bool ready = false;
   bool supported = false;
   int sm_count = 0;
-  bool attr_set[3] = {false, false, false};  // D = 32, 64, 128
+  bool attr_set[6] = {};  // D = 32, 64, 128; bf16 or e4m3 Q/K
 };
 
 std::mutex g_mutex;
@@ -43,6 +44,8 @@ bool ranges_overlap(const void* a, size_t abytes, const void* b, size_t bbytes) 
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 unsigned long long timeout_ns_from_env() {
   const char* e = std::getenv("FA_WAIT_TIMEOUT_MS");
@@ -100,27 +103,27 @@ int encode_map(CUtensorMap* map, const void* base, int BH, int N, int D) {
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
 
-template <int D>
+template <int D, bool F8>
 int launch(const fa::Params& prm, DeviceState& st, int slot, cudaStream_t stream) {
-  using C = fa::Cfg<D>;
+  using C = fa::Cfg<D, F8>;
   {
     std::lock_guard<std::mutex> lock(g_mutex);
     if (!st.attr_set[slot]) {
-      if (cudaFuncSetAttribute(fa::fa_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      if (cudaFuncSetAttribute(fa::fa_fwd_kernel<D, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                C::SMEM_BYTES) != cudaSuccess)
         return FA_ERR_CUDA;
       // The warpgroup register split (setmaxnreg) must fit in the registers
       // the launch reserves, or the increase would wait forever: refuse to
       // launch a build where it does not.
       cudaFuncAttributes fattr;
-      if (cudaFuncGetAttributes(&fattr, fa::fa_fwd_kernel<D>) != cudaSuccess) return FA_ERR_CUDA;
+      if (cudaFuncGetAttributes(&fattr, fa::fa_fwd_kernel<D, F8>) != cudaSuccess) return FA_ERR_CUDA;
       if (2 * 128 * C::REGS_SOFTMAX + 128 * C::REGS_OTHER > fattr.numRegs * C::THREADS)
         return FA_ERR_UNSUPPORTED;
       st.attr_set[slot] = true;
     }
   }
   const int grid = prm.num_units < st.sm_count ? prm.num_units : st.sm_count;
-  fa::fa_fwd_kernel<D><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(prm);
+  fa::fa_fwd_kernel<D, F8><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(prm);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -196,19 +199,82 @@ int prepare(const void* q, const void* k, const void* v, const float* mask, void
   return FA_OK;
 }
 
-int launch_fwd(const fa::Params& prm, DeviceState& st, int D, cudaStream_t s) {
-  switch (D) {
-    case 32: return launch<32>(prm, st, 0, s);
-    case 64: return launch<64>(prm, st, 1, s);
-    default: return launch<128>(prm, st, 2, s);
+int launch_fwd(const fa::Params& prm, DeviceState& st, int D, cudaStream_t s, bool f8 = false) {
+  if (f8) {
+    switch (D) {
+      case 32: return launch<32, true>(prm, st, 3, s);
+      case 64: return launch<64, true>(prm, st, 4, s);
+      default: return launch<128, true>(prm, st, 5, s);
+    }
   }
+  switch (D) {
+    case 32: return launch<32, false>(prm, st, 0, s);
+    case 64: return launch<64, false>(prm, st, 1, s);
+    default: return launch<128, false>(prm, st, 2, s);
+  }
+}
+
+// 3-D tensor map over a contiguous e4m3 [BH][N][D] tensor: one box row is the
+// whole D-byte row, swizzled over D bytes (128 / 64 / 32).
+int encode_map_f8(CUtensorMap* map, const void* base, int BH, int N, int D) {
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)N, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)D, (cuuint64_t)N * D};
+  cuuint32_t box[3] = {(cuuint32_t)D, 128u, 1u};
+  cuuint32_t estride[3] = {1u, 1u, 1u};
+  const CUtensorMapSwizzle sw = D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                         : (D == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides,
+                        box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
+// Workspace of the FP8 forward, in order (each part 256-byte aligned).
+struct F8Layout {
+  size_t q8, k8, q_scale, k_scale, mean, partial, corr, total;
+};
+constexpr int kF8ColsumSplits = 64;
+
+F8Layout f8_layout(int B, int H, int Nq, int Nk, int D) {
+  const size_t BH = (size_t)B * H;
+  const size_t qt = ((size_t)Nq + 127) / 128, kt = ((size_t)Nk + 127) / 128;
+  F8Layout l{};
+  size_t off = 0;
+  l.q8 = off;       off += align256(BH * Nq * D);
+  l.k8 = off;       off += align256(BH * Nk * D);
+  l.q_scale = off;  off += align256(BH * qt * 4);
+  l.k_scale = off;  off += align256(BH * kt * 4);
+  l.mean = off;     off += align256(BH * D * 4);
+  l.partial = off;  off += align256(BH * kF8ColsumSplits * D * 4);
+  l.corr = off;     off += align256(BH * Nq * 4);
+  l.total = off;
+  return l;
+}
+
+template <int D>
+void launch_quant(const void* q, const void* k, char* ws, const F8Layout& L, int BH, int Nq, int Nk,
+                  float scale, cudaStream_t s) {
+  fa::fa_k_colsum_kernel<D><<<dim3(BH, kF8ColsumSplits), 256, 0, s>>>(
+      static_cast<const __nv_bfloat16*>(k), reinterpret_cast<float*>(ws + L.partial), Nk,
+      kF8ColsumSplits);
+  fa::fa_k_mean_kernel<<<(BH * D + 255) / 256, 256, 0, s>>>(
+      reinterpret_cast<const float*>(ws + L.partial), reinterpret_cast<float*>(ws + L.mean), BH, D,
+      kF8ColsumSplits, Nk);
+  const int kt = (Nk + 127) / 128, qt = (Nq + 127) / 128;
+  fa::fa_quant_rows_kernel<D, true><<<BH * kt, 128, 0, s>>>(
+      static_cast<const __nv_bfloat16*>(k), reinterpret_cast<const float*>(ws + L.mean),
+      reinterpret_cast<uint8_t*>(ws + L.k8), reinterpret_cast<float*>(ws + L.k_scale), nullptr, Nk,
+      kt, scale);
+  fa::fa_quant_rows_kernel<D, false><<<BH * qt, 128, 0, s>>>(
+      static_cast<const __nv_bfloat16*>(q), reinterpret_cast<const float*>(ws + L.mean),
+      reinterpret_cast<uint8_t*>(ws + L.q8), reinterpret_cast<float*>(ws + L.q_scale),
+      reinterpret_cast<float*>(ws + L.corr), Nq, qt, scale);
 }
 
 // Key ranges actually used for a requested count: at most one per key block,
 // so that every range is non-empty.
 int effective_splits(int nkv, int requested) { return requested < nkv ? requested : nkv; }
 
-size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 }  // namespace
 
@@ -255,6 +321,49 @@ int fa_fwd_ex(const void* q, const void* k, const void* v, const fa_mask* mask, 
   }
   prm.causal = causal ? 1 : 0;
   return launch_fwd(prm, *st, D, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t fa_fp8_workspace_bytes(int B, int H, int Nq, int Nk, int D) {
+  if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || (D != 32 && D != 64 && D != 128)) return 0;
+  return f8_layout(B, H, Nq, Nk, D).total;
+}
+
+int fa_fwd_fp8(const void* q, const void* k, const void* v, const float* mask, void* out,
+               float* lse, int B, int H, int Nq, int Nk, int D, float scale, void* workspace,
+               size_t workspace_bytes, void* stream) {
+  if (!workspace || !aligned16(workspace)) return FA_ERR_INVALID_ARGUMENT;
+  if (B >= 1 && H >= 1 && Nq >= 1 && Nk >= 1 && (D == 32 || D == 64 || D == 128) &&
+      workspace_bytes < fa_fp8_workspace_bytes(B, H, Nq, Nk, D))
+    return FA_ERR_INVALID_ARGUMENT;
+  fa::Params prm;
+  DeviceState* st = nullptr;
+  int rc = prepare(q, k, v, mask, out, lse, B, H, Nq, Nk, D, scale, &prm, &st);
+  if (rc != FA_OK) return rc;
+  const F8Layout L = f8_layout(B, H, Nq, Nk, D);
+  const size_t rows = (size_t)prm.BH * Nq;
+  if (ranges_overlap(workspace, L.total, q, rows * D * 2) ||
+      ranges_overlap(workspace, L.total, k, (size_t)prm.BH * Nk * D * 2) ||
+      ranges_overlap(workspace, L.total, v, (size_t)prm.BH * Nk * D * 2) ||
+      ranges_overlap(workspace, L.total, out, rows * D * 2) ||
+      ranges_overlap(workspace, L.total, lse, rows * 4) ||
+      ranges_overlap(workspace, L.total, mask, mask ? (size_t)B * Nk * 4 : 0))
+    return FA_ERR_INVALID_ARGUMENT;
+  char* ws = static_cast<char*>(workspace);
+  if (encode_map_f8(&prm.tm_q, ws + L.q8, prm.BH, Nq, D) != FA_OK ||
+      encode_map_f8(&prm.tm_k, ws + L.k8, prm.BH, Nk, D) != FA_OK)
+    return FA_ERR_CUDA;
+  prm.q_scale = reinterpret_cast<const float*>(ws + L.q_scale);
+  prm.k_scale = reinterpret_cast<const float*>(ws + L.k_scale);
+  prm.lse_corr = reinterpret_cast<const float*>(ws + L.corr);
+  prm.qtiles = (Nq + 127) / 128;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  switch (D) {
+    case 32: launch_quant<32>(q, k, ws, L, prm.BH, Nq, Nk, scale, s); break;
+    case 64: launch_quant<64>(q, k, ws, L, prm.BH, Nq, Nk, scale, s); break;
+    default: launch_quant<128>(q, k, ws, L, prm.BH, Nq, Nk, scale, s); break;
+  }
+  if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+  return launch_fwd(prm, *st, D, s, true);
 }
 
 size_t fa_split_workspace_bytes(int B, int H, int Nq, int D, int num_splits) {

@@ -39,22 +39,35 @@ constexpr uint32_t kSuspendNs = 20000;  // longest sleep inside one mbarrier pol
 // Device status word (one per device per loaded library): 0 or a status code.
 __device__ int g_device_status = 0;
 
-template <int D>
+// F8: Q and K are e4m3 (one byte) with per-128-row block scales and
+// S = Q K^T runs as kind::f8f6f4 MMAs; V and P stay bf16.
+template <int D, bool F8 = false>
 struct Cfg {
   static_assert(D == 32 || D == 64 || D == 128, "head dim");
   static constexpr int BM = 128;                       // query rows per tile
   static constexpr int BN = 128;                       // keys per tile
+  // bf16 tiles (V always; Q and K without F8)
   static constexpr int SW = (D >= 64) ? 128 : 64;      // swizzle span = bytes per chunk row
   static constexpr int CHUNK_ELEMS = SW / 2;           // bf16 per chunk row
   static constexpr int NCHUNK = D / CHUNK_ELEMS;       // chunks across the head dim
   static constexpr int CHUNK_BYTES = BN * SW;          // one 128-row chunk
-  static constexpr int TILE_BYTES = BN * D * 2;        // one 128-row tile (Q, K or V)
+  static constexpr int TILE_BYTES = BN * D * 2;        // one 128-row bf16 tile = one ring stage
+  // Q and K tiles (operands of S = Q K^T)
+  static constexpr int QK_ELEM = F8 ? 1 : 2;
+  static constexpr int QK_SW = F8 ? D : SW;            // fp8 rows are D bytes: 128/64/32-byte swizzle
+  static constexpr int QK_CHUNK_ELEMS = QK_SW / QK_ELEM;
+  static constexpr int QK_NCHUNK = D / QK_CHUNK_ELEMS;
+  static constexpr int QK_CHUNK_BYTES = BN * QK_SW;
+  static constexpr int QK_TILE_BYTES = BN * D * QK_ELEM;
+  static constexpr int QK_SBO = 8 * QK_SW;
+  static constexpr uint32_t QK_LAYOUT = QK_SW == 128 ? 2u : (QK_SW == 64 ? 4u : 6u);
+  static constexpr int QK_KSTEP = F8 ? 32 : 16;        // K elements per MMA instruction
 #ifndef FA_STAGES_D128
 #define FA_STAGES_D128 5
 #endif
   // K/V ring depth: as deep as shared memory allows (227 KB per CTA).
-  static constexpr int STAGES = (D == 128) ? FA_STAGES_D128 : (D == 64 ? 6 : 8);
-  static constexpr int SMEM_Q = 2 * TILE_BYTES;
+  static constexpr int STAGES = (D == 128) ? (F8 ? 6 : FA_STAGES_D128) : (D == 64 ? 6 : 8);
+  static constexpr int SMEM_Q = 2 * QK_TILE_BYTES;
   static constexpr int SMEM_RING = STAGES * TILE_BYTES;
   static constexpr int SMEM_BAR = 1024;
   static constexpr int SMEM_USED = 1024 /*align slack*/ + SMEM_Q + SMEM_RING + SMEM_BAR;
@@ -99,6 +112,10 @@ struct Params {  // 64-byte aligned through its CUtensorMap members
   float* part_o;       // split mode: fp32 [num_splits][BH][Nq][D] partial O (else nullptr)
   float* part_lse;     // split mode: fp32 [num_splits][BH][Nq] partial LSE
   float scale_log2;    // scale * log2(e)
+  const float* q_scale;   // F8: [BH][ceil(Nq/128)] e4m3 block scale of Q
+  const float* k_scale;   // F8: [BH][nkv] e4m3 block scale of the smoothed K
+  const float* lse_corr;  // F8: [BH][Nq] scale * q_i . mean(K), added back to LSE
+  int qtiles;             // ceil(Nq/128)
   unsigned long long timeout_ns;
   int inject_stall;    // test hook: CTA 0's producer withholds its 4th K/V tile
 };
@@ -146,6 +163,12 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
 __host__ __device__ constexpr uint32_t make_idesc(int M, int N, bool b_mn_major) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
          ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// Instruction descriptor for kind::f8f6f4 with e4m3 A/B (format 0), K-major,
+// fp32 accumulate.
+__host__ __device__ constexpr uint32_t make_idesc_f8(int M, int N) {
+  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 struct Barriers {
@@ -216,10 +239,10 @@ __device__ __forceinline__ float2 exp2_fma_pipe(float2 x) {
   return make_float2(__uint_as_float(b0), __uint_as_float(b1));
 }
 
-template <int D>
-__global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
+template <int D, bool F8>
+__global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
     fa_fwd_kernel(const __grid_constant__ Params p) {
-  using C = Cfg<D>;
+  using C = Cfg<D, F8>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -287,11 +310,11 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         ok = bounded_wait(ptx::smem_u32(&bars->q_empty), (uc & 1) ^ 1, bars, p.timeout_ns);
         if (!ok) break;
         const uint32_t qbar = ptx::smem_u32(&bars->q_full);
-        ptx::mbar_arrive_expect_tx(qbar, ntiles * C::TILE_BYTES);
+        ptx::mbar_arrive_expect_tx(qbar, ntiles * C::QK_TILE_BYTES);
         for (int t = 0; t < ntiles; ++t)
-          for (int c = 0; c < C::NCHUNK; ++c)
-            ptx::tma_load_3d(ptx::smem_u32(sQ + t * C::TILE_BYTES + c * C::CHUNK_BYTES), &p.tm_q,
-                             qbar, c * C::CHUNK_ELEMS, q0 + t * 128, bh);
+          for (int c = 0; c < C::QK_NCHUNK; ++c)
+            ptx::tma_load_3d(ptx::smem_u32(sQ + t * C::QK_TILE_BYTES + c * C::QK_CHUNK_BYTES),
+                             &p.tm_q, qbar, c * C::QK_CHUNK_ELEMS, q0 + t * 128, bh);
         ++q_issued;
         for (int j = 0; j < un.ntiles && ok; ++j) {
           for (int kv = 0; kv < 2; ++kv, ++it) {
@@ -301,11 +324,17 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
             if (!ok) break;
             const uint32_t fb = ptx::smem_u32(&bars->kv_full[s]);
             if (p.inject_stall && blockIdx.x == 0 && it == 3) continue;  // nothing arrives: consumers time out
-            ptx::mbar_arrive_expect_tx(fb, C::TILE_BYTES);
-            const void* tm = kv == 0 ? (const void*)&p.tm_k : (const void*)&p.tm_v;
-            for (int c = 0; c < C::NCHUNK; ++c)
-              ptx::tma_load_3d(ptx::smem_u32(sRing + s * C::TILE_BYTES + c * C::CHUNK_BYTES), tm,
-                               fb, c * C::CHUNK_ELEMS, (un.tile0 + j) * 128, bh);
+            if (kv == 0) {
+              ptx::mbar_arrive_expect_tx(fb, C::QK_TILE_BYTES);
+              for (int c = 0; c < C::QK_NCHUNK; ++c)
+                ptx::tma_load_3d(ptx::smem_u32(sRing + s * C::TILE_BYTES + c * C::QK_CHUNK_BYTES),
+                                 &p.tm_k, fb, c * C::QK_CHUNK_ELEMS, (un.tile0 + j) * 128, bh);
+            } else {
+              ptx::mbar_arrive_expect_tx(fb, C::TILE_BYTES);
+              for (int c = 0; c < C::NCHUNK; ++c)
+                ptx::tma_load_3d(ptx::smem_u32(sRing + s * C::TILE_BYTES + c * C::CHUNK_BYTES),
+                                 &p.tm_v, fb, c * C::CHUNK_ELEMS, (un.tile0 + j) * 128, bh);
+            }
             ++issued[s];
           }
         }
@@ -334,7 +363,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
   } else if (warp == 9) {
     // ----------------------------------------------------------------- MMA --
     if (lane == 0) {
-      constexpr uint32_t IDESC_QK = make_idesc(128, 128, false);
+      constexpr uint32_t IDESC_QK = F8 ? make_idesc_f8(128, 128) : make_idesc(128, 128, false);
       constexpr uint32_t IDESC_PV = make_idesc(128, D, true);
       const uint32_t sq = ptx::smem_u32(sQ);
       const uint32_t sring = ptx::smem_u32(sRing);
@@ -345,21 +374,26 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       // Shared-memory descriptors are built once; per k-step only the start
       // address (low 14 bits, in 16-byte units) moves, which never carries
       // out of its field because shared memory is below 256 KB.
-      constexpr uint32_t kTile16 = C::TILE_BYTES >> 4;
-      const uint64_t dq0 = smem_desc(sq, 16, C::SBO, C::LAYOUT);
-      const uint64_t dk0 = smem_desc(sring, 16, C::SBO, C::LAYOUT);
+      constexpr uint32_t kTile16 = C::TILE_BYTES >> 4;       // ring stage stride
+      constexpr uint32_t kQTile16 = C::QK_TILE_BYTES >> 4;   // Q tile stride
+      const uint64_t dq0 = smem_desc(sq, 16, C::QK_SBO, C::QK_LAYOUT);
+      const uint64_t dk0 = smem_desc(sring, 16, C::QK_SBO, C::QK_LAYOUT);
       const uint64_t dv0 = smem_desc(sring, C::CHUNK_BYTES, C::SBO, C::LAYOUT);
 
       // S_t = Q_t K^T : A = Q tile (K-major), B = K tile (K-major), K-dim = D.
       auto issue_s = [&](int t, uint32_t stg) {
-        const uint64_t a = dq0 + (uint64_t)(t * kTile16);
+        const uint64_t a = dq0 + (uint64_t)(t * kQTile16);
         const uint64_t b = dk0 + (uint64_t)(stg * kTile16);
         const uint32_t d = tmem + (t ? C::COL_S1 : C::COL_S0);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          constexpr int kPerChunk = C::CHUNK_ELEMS / 16;
-          const uint32_t off = ((kk / kPerChunk) * C::CHUNK_BYTES + (kk % kPerChunk) * 32) >> 4;
-          ptx::mma_ss(d, a + off, b + off, IDESC_QK, kk > 0);
+        for (int kk = 0; kk < D / C::QK_KSTEP; ++kk) {
+          constexpr int kPerChunk = C::QK_CHUNK_ELEMS / C::QK_KSTEP;
+          // every k-step covers 32 bytes of a row (16 bf16 or 32 e4m3)
+          const uint32_t off = ((kk / kPerChunk) * C::QK_CHUNK_BYTES + (kk % kPerChunk) * 32) >> 4;
+          if constexpr (F8)
+            ptx::mma_ss_f8(d, a + off, b + off, IDESC_QK, kk > 0);
+          else
+            ptx::mma_ss(d, a + off, b + off, IDESC_QK, kk > 0);
         }
       };
       // O_t += P_t V : A = P (tensor memory, over the S_t block), B = V tile
@@ -499,11 +533,17 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
           for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(r[c]);
         }
         const int kbase = (un.tile0 + j) * 128;
+        // log2-domain multiplier of raw S; with e4m3 Q and K it carries the
+        // two block scales (positive, so its sign is the sign of `scale`).
+        float sl2 = scale_log2;
+        if constexpr (F8)
+          sl2 *= __ldg(p.q_scale + (size_t)bh * p.qtiles + (tile_row0 >> 7)) *
+                 __ldg(p.k_scale + (size_t)bh * p.nkv + un.tile0 + j);
         // Fast path: full key block, no mask, non-negative scale — the row max
         // is taken on raw scores and scaled once.  Otherwise scores are
         // materialised in the log2 domain with the mask and the Nk tail.
         const bool general = (mask_b != nullptr) || any_full_mask || (kbase + 128 > p.Nk) ||
-                             !(scale_log2 >= 0.f) || (p.causal && kbase + 127 > tile_row0);
+                             !(sl2 >= 0.f) || (p.causal && kbase + 127 > tile_row0);
         float mx;
         if (!general) {
           float a0 = s[0], a1 = s[1], a2 = s[2], a3 = s[3];
@@ -514,7 +554,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
             a2 = ptx::fmax3(a2, s[c + 4], s[c + 5]);
             a3 = ptx::fmax3(a3, s[c + 6], s[c + 7]);
           }
-          mx = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)) * scale_log2;
+          mx = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)) * sl2;
         } else {
           mx = -INFINITY;
           // This row of the per-(query, key) mask (rows past Nq read nothing).
@@ -534,7 +574,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
             const int key = kbase + c;
             float tv = -INFINITY;
             if (key < p.Nk && !(p.causal && key > qrow)) {
-              tv = s[c] * scale_log2;
+              tv = s[c] * sl2;
               if (mask_b) tv = fmaf(__ldg(mask_b + key), kLog2e, tv);
               if (fmask_f) tv = fmaf(__ldg(fmask_f + key), kLog2e, tv);
               if (fmask_b && __ldg(fmask_b + key) == 0) tv = -INFINITY;
@@ -557,7 +597,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         l *= alpha;
         float2 lsum = make_float2(0.f, 0.f);
         if (!general) {
-          const float2 sc2 = make_float2(scale_log2, scale_log2);
+          const float2 sc2 = make_float2(sl2, sl2);
           const float2 nm2 = make_float2(-m_use, -m_use);
 #pragma unroll
           for (int cb = 0; cb < 128; cb += 32) {
@@ -618,7 +658,11 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
       const bool valid_row = qrow < p.Nq;
       constexpr float kLn2 = 0.6931471805599453f;
-      const float row_lse = (l > 0.f) ? (m + __log2f(l)) * kLn2 : -INFINITY;
+      float row_lse = (l > 0.f) ? (m + __log2f(l)) * kLn2 : -INFINITY;
+      if constexpr (F8) {
+        // K was smoothed by its per-channel mean: add back scale * q_i . mean(K).
+        if (valid_row) row_lse += __ldg(p.lse_corr + (size_t)bh * p.Nq + qrow);
+      }
       if (p.part_o == nullptr) {
         __nv_bfloat16* orow = p.out + ((size_t)bh * p.Nq + (valid_row ? qrow : 0)) * D;
 #pragma unroll
