@@ -62,6 +62,13 @@ struct Cfg {
   static constexpr int QK_SBO = 8 * QK_SW;
   static constexpr uint32_t QK_LAYOUT = QK_SW == 128 ? 2u : (QK_SW == 64 ? 4u : 6u);
   static constexpr int QK_KSTEP = F8 ? 32 : 16;        // K elements per MMA instruction
+  static constexpr int S_MMAS = D / QK_KSTEP;          // MMA instructions per S tile
+  // Start-address offset (16-byte units) of k-step kk of S = Q K^T: each
+  // k-step covers 32 bytes of a row (16 bf16 or 32 e4m3).
+  __host__ __device__ static constexpr uint32_t s_off(int kk) {
+    return ((kk / (QK_CHUNK_ELEMS / QK_KSTEP)) * QK_CHUNK_BYTES +
+            (kk % (QK_CHUNK_ELEMS / QK_KSTEP)) * 32) >> 4;
+  }
 #ifndef FA_STAGES_D128
 #define FA_STAGES_D128 5
 #endif
@@ -380,33 +387,40 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
       const uint64_t dk0 = smem_desc(sring, 16, C::QK_SBO, C::QK_LAYOUT);
       const uint64_t dv0 = smem_desc(sring, C::CHUNK_BYTES, C::SBO, C::LAYOUT);
 
-      // S_t = Q_t K^T : A = Q tile (K-major), B = K tile (K-major), K-dim = D.
+      const uint32_t dq_lo = (uint32_t)dq0, dq_hi = (uint32_t)(dq0 >> 32);
+      const uint32_t dk_lo = (uint32_t)dk0, dk_hi = (uint32_t)(dk0 >> 32);
+      const uint32_t dv_lo = (uint32_t)dv0, dv_hi = (uint32_t)(dv0 >> 32);
+
+      // S_t = Q_t K^T : A = Q tile (K-major), B = K tile (K-major), K-dim = D;
+      // one asm block per tile (the first MMA overwrites S).
       auto issue_s = [&](int t, uint32_t stg) {
-        const uint64_t a = dq0 + (uint64_t)(t * kQTile16);
-        const uint64_t b = dk0 + (uint64_t)(stg * kTile16);
+        const uint32_t a = dq_lo + t * kQTile16;
+        const uint32_t b = dk_lo + stg * kTile16;
         const uint32_t d = tmem + (t ? C::COL_S1 : C::COL_S0);
-#pragma unroll
-        for (int kk = 0; kk < D / C::QK_KSTEP; ++kk) {
-          constexpr int kPerChunk = C::QK_CHUNK_ELEMS / C::QK_KSTEP;
-          // every k-step covers 32 bytes of a row (16 bf16 or 32 e4m3)
-          const uint32_t off = ((kk / kPerChunk) * C::QK_CHUNK_BYTES + (kk % kPerChunk) * 32) >> 4;
-          if constexpr (F8)
-            ptx::mma_ss_f8(d, a + off, b + off, IDESC_QK, kk > 0);
+        if constexpr (F8) {
+          if constexpr (C::S_MMAS == 4)
+            ptx::mma_ss_f8_x4<C::s_off(1), C::s_off(2), C::s_off(3)>(d, a, dq_hi, b, dk_hi, IDESC_QK, 0);
+          else if constexpr (C::S_MMAS == 2)
+            ptx::mma_ss_f8_x2<C::s_off(1)>(d, a, dq_hi, b, dk_hi, IDESC_QK, 0);
           else
-            ptx::mma_ss(d, a + off, b + off, IDESC_QK, kk > 0);
+            ptx::mma_ss_f8_x1(d, a, dq_hi, b, dk_hi, IDESC_QK, 0);
+        } else {
+          if constexpr (C::S_MMAS == 8)
+            ptx::mma_ss_x8<C::s_off(1), C::s_off(2), C::s_off(3), C::s_off(4), C::s_off(5),
+                           C::s_off(6), C::s_off(7)>(d, a, dq_hi, b, dk_hi, IDESC_QK, 0);
+          else if constexpr (C::S_MMAS == 4)
+            ptx::mma_ss_x4<C::s_off(1), C::s_off(2), C::s_off(3)>(d, a, dq_hi, b, dk_hi, IDESC_QK, 0);
+          else
+            ptx::mma_ss_x2<C::s_off(1)>(d, a, dq_hi, b, dk_hi, IDESC_QK, 0);
         }
       };
       // O_t += P_t V : A = P (tensor memory, over the S_t block), B = V tile
-      // (MN-major: the head dim is contiguous), K-dim = 128 keys.
+      // (MN-major: the head dim is contiguous), K-dim = 128 keys in 8 MMAs.
       auto issue_pv = [&](int t, uint32_t stg, bool first) {
-        const uint64_t b = dv0 + (uint64_t)(stg * kTile16);
+        const uint32_t b = dv_lo + stg * kTile16;
         const uint32_t a_tmem = tmem + (t ? C::COL_S1 : C::COL_S0);
         const uint32_t d = tmem + (t ? C::COL_O1 : C::COL_O0);
-#pragma unroll
-        for (int kk = 0; kk < 128 / 16; ++kk) {
-          ptx::mma_ts(d, a_tmem + kk * 8, b + (uint64_t)((kk * 16 * C::SW) >> 4), IDESC_PV,
-                      (!first || kk > 0) ? 1u : 0u);
-        }
+        ptx::mma_ts_x8<((16 * C::SW) >> 4)>(d, a_tmem, b, dv_hi, IDESC_PV, first ? 0u : 1u);
       };
       // Wait until the ring's current stage is full; returns that stage.
       auto take_stage = [&](uint32_t& stg) -> bool {
