@@ -14,7 +14,8 @@
 //   warps 0-3  softmax warpgroup for query tile 0 (one thread per row)
 //   warps 4-7  softmax warpgroup for query tile 1
 //   warp  8    TMA producer: Q tiles, then K_j, V_j into a shared-memory ring
-//   warp  9    MMA issuer (one thread) and TMEM owner
+//   warp  9    MMA issuer and TMEM owner (the warp runs the loop, one elected
+//              lane issues each MMA batch and commit)
 //   warps 10-11 idle
 // Tensor memory (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+D),
 // O1 [256+D, 256+2D).  P (bf16) is written over the first 64 columns of its
@@ -369,7 +370,9 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
     __syncwarp();
   } else if (warp == 9) {
     // ----------------------------------------------------------------- MMA --
-    if (lane == 0) {
+    // The whole warp runs the loop (operands warp-uniform); one elected lane
+    // issues each MMA batch and commit.
+    {
       constexpr uint32_t IDESC_QK = F8 ? make_idesc_f8(128, 128) : make_idesc(128, 128, false);
       constexpr uint32_t IDESC_PV = make_idesc(128, D, true);
       const uint32_t sq = ptx::smem_u32(sQ);
@@ -399,19 +402,19 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
         const uint32_t d = tmem + (t ? C::COL_S1 : C::COL_S0);
         if constexpr (F8) {
           if constexpr (C::S_MMAS == 4)
-            ptx::mma_ss_f8_x4<C::s_off(1), C::s_off(2), C::s_off(3)>(d, a, dq_hi, b, dk_hi, IDESC_QK, 0);
+            ptx::mma_ss_f8_x4_el<C::s_off(1), C::s_off(2), C::s_off(3)>(d, a, dq_hi, b, dk_hi, IDESC_QK, 0);
           else if constexpr (C::S_MMAS == 2)
-            ptx::mma_ss_f8_x2<C::s_off(1)>(d, a, dq_hi, b, dk_hi, IDESC_QK, 0);
+            ptx::mma_ss_f8_x2_el<C::s_off(1)>(d, a, dq_hi, b, dk_hi, IDESC_QK, 0);
           else
-            ptx::mma_ss_f8_x1(d, a, dq_hi, b, dk_hi, IDESC_QK, 0);
+            ptx::mma_ss_f8_x1_el(d, a, dq_hi, b, dk_hi, IDESC_QK, 0);
         } else {
           if constexpr (C::S_MMAS == 8)
-            ptx::mma_ss_x8<C::s_off(1), C::s_off(2), C::s_off(3), C::s_off(4), C::s_off(5),
+            ptx::mma_ss_x8_el<C::s_off(1), C::s_off(2), C::s_off(3), C::s_off(4), C::s_off(5),
                            C::s_off(6), C::s_off(7)>(d, a, dq_hi, b, dk_hi, IDESC_QK, 0);
           else if constexpr (C::S_MMAS == 4)
-            ptx::mma_ss_x4<C::s_off(1), C::s_off(2), C::s_off(3)>(d, a, dq_hi, b, dk_hi, IDESC_QK, 0);
+            ptx::mma_ss_x4_el<C::s_off(1), C::s_off(2), C::s_off(3)>(d, a, dq_hi, b, dk_hi, IDESC_QK, 0);
           else
-            ptx::mma_ss_x2<C::s_off(1)>(d, a, dq_hi, b, dk_hi, IDESC_QK, 0);
+            ptx::mma_ss_x2_el<C::s_off(1)>(d, a, dq_hi, b, dk_hi, IDESC_QK, 0);
         }
       };
       // O_t += P_t V : A = P (tensor memory, over the S_t block), B = V tile
@@ -420,12 +423,12 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
         const uint32_t b = dv_lo + stg * kTile16;
         const uint32_t a_tmem = tmem + (t ? C::COL_S1 : C::COL_S0);
         const uint32_t d = tmem + (t ? C::COL_O1 : C::COL_O0);
-        ptx::mma_ts_x8<((16 * C::SW) >> 4)>(d, a_tmem, b, dv_hi, IDESC_PV, first ? 0u : 1u);
+        ptx::mma_ts_x8_el<((16 * C::SW) >> 4)>(d, a_tmem, b, dv_hi, IDESC_PV, first ? 0u : 1u);
       };
       // Wait until the ring's current stage is full; returns that stage.
       auto take_stage = [&](uint32_t& stg) -> bool {
         stg = stage;
-        const bool r = bounded_wait(ptx::smem_u32(&bars->kv_full[stage]), phase, bars, p.timeout_ns);
+        const bool r = bounded_wait_warp(ptx::smem_u32(&bars->kv_full[stage]), phase, bars, p.timeout_ns);
         if (++stage == (uint32_t)C::STAGES) {
           stage = 0;
           phase ^= 1u;
@@ -438,7 +441,7 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
         const Unit un = decode_unit(p, u);
         const bool has1 = un.q0 + 128 < p.Nq;
         const int nkv = un.ntiles;
-        ok = bounded_wait(ptx::smem_u32(&bars->q_full), uc & 1, bars, p.timeout_ns);
+        ok = bounded_wait_warp(ptx::smem_u32(&bars->q_full), uc & 1, bars, p.timeout_ns);
         if (!ok) break;
         ptx::tc_fence_after_sync();
         // Prologue: S for key block 0.
@@ -446,53 +449,53 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
         ok = take_stage(sK);
         if (!ok) break;
         issue_s(0, sK);
-        ptx::mma_commit(ptx::smem_u32(&bars->s_full[0]));
+        ptx::mma_commit_el(ptx::smem_u32(&bars->s_full[0]));
         if (has1) {
           issue_s(1, sK);
-          ptx::mma_commit(ptx::smem_u32(&bars->s_full[1]));
+          ptx::mma_commit_el(ptx::smem_u32(&bars->s_full[1]));
         }
-        ptx::mma_commit(ptx::smem_u32(&bars->kv_empty[sK]));
-        if (nkv == 1) ptx::mma_commit(ptx::smem_u32(&bars->q_empty));
+        ptx::mma_commit_el(ptx::smem_u32(&bars->kv_empty[sK]));
+        if (nkv == 1) ptx::mma_commit_el(ptx::smem_u32(&bars->q_empty));
 
         for (int j = 0; j < nkv && ok; ++j) {
           ok = take_stage(sV);
           if (!ok) break;
           const bool has_next = j + 1 < nkv;
           // O0 += P0 V_j
-          ok = bounded_wait(ptx::smem_u32(&bars->p_ready[0]), pc0 & 1, bars, p.timeout_ns);
+          ok = bounded_wait_warp(ptx::smem_u32(&bars->p_ready[0]), pc0 & 1, bars, p.timeout_ns);
           if (!ok) break;
           ++pc0;
           ptx::tc_fence_after_sync();
           issue_pv(0, sV, j == 0);
-          if (!has_next) ptx::mma_commit(ptx::smem_u32(&bars->o_full[0]));
+          if (!has_next) ptx::mma_commit_el(ptx::smem_u32(&bars->o_full[0]));
           // S0 for key block j+1 as soon as P0 has been consumed.
           if (has_next) {
             ok = take_stage(sK);
             if (!ok) break;
             issue_s(0, sK);
-            ptx::mma_commit(ptx::smem_u32(&bars->s_full[0]));
+            ptx::mma_commit_el(ptx::smem_u32(&bars->s_full[0]));
           }
           if (has1) {
-            ok = bounded_wait(ptx::smem_u32(&bars->p_ready[1]), pc1 & 1, bars, p.timeout_ns);
+            ok = bounded_wait_warp(ptx::smem_u32(&bars->p_ready[1]), pc1 & 1, bars, p.timeout_ns);
             if (!ok) break;
             ++pc1;
             ptx::tc_fence_after_sync();
             issue_pv(1, sV, j == 0);
-            if (!has_next) ptx::mma_commit(ptx::smem_u32(&bars->o_full[1]));
+            if (!has_next) ptx::mma_commit_el(ptx::smem_u32(&bars->o_full[1]));
           }
-          ptx::mma_commit(ptx::smem_u32(&bars->kv_empty[sV]));
+          ptx::mma_commit_el(ptx::smem_u32(&bars->kv_empty[sV]));
           if (has_next) {
             if (has1) {
               issue_s(1, sK);
-              ptx::mma_commit(ptx::smem_u32(&bars->s_full[1]));
+              ptx::mma_commit_el(ptx::smem_u32(&bars->s_full[1]));
             }
-            ptx::mma_commit(ptx::smem_u32(&bars->kv_empty[sK]));
-            if (j + 2 == nkv) ptx::mma_commit(ptx::smem_u32(&bars->q_empty));
+            ptx::mma_commit_el(ptx::smem_u32(&bars->kv_empty[sK]));
+            if (j + 2 == nkv) ptx::mma_commit_el(ptx::smem_u32(&bars->q_empty));
           }
         }
       }
       // Drain this thread's MMAs before tensor memory can be freed.
-      ptx::mma_commit(ptx::smem_u32(&bars->drain));
+      ptx::mma_commit_el(ptx::smem_u32(&bars->drain));
       {
         const uint32_t bar = ptx::smem_u32(&bars->drain);
         uint64_t t0 = ptx::global_timer_ns();
