@@ -181,7 +181,7 @@ __host__ __device__ constexpr uint32_t make_idesc_f8(int M, int N) {
 
 struct Barriers {
   uint64_t q_full, q_empty;
-  uint64_t s_full[2], p_ready[2], o_full[2];
+  uint64_t s_full[2], p_half[2], p_ready[2], o_full[2];
   uint64_t drain;
   uint32_t tmem_base;
   volatile int abort_flag;
@@ -266,6 +266,7 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
     ptx::mbar_init(ptx::smem_u32(&bars->q_empty), 1);
     for (int t = 0; t < 2; ++t) {
       ptx::mbar_init(ptx::smem_u32(&bars->s_full[t]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bars->p_half[t]), 128);
       ptx::mbar_init(ptx::smem_u32(&bars->p_ready[t]), 128);
       ptx::mbar_init(ptx::smem_u32(&bars->o_full[t]), 1);
     }
@@ -418,12 +419,28 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
         }
       };
       // O_t += P_t V : A = P (tensor memory, over the S_t block), B = V tile
-      // (MN-major: the head dim is contiguous), K-dim = 128 keys in 8 MMAs.
-      auto issue_pv = [&](int t, uint32_t stg, bool first) {
-        const uint32_t b = dv_lo + stg * kTile16;
-        const uint32_t a_tmem = tmem + (t ? C::COL_S1 : C::COL_S0);
+      // (MN-major: the head dim is contiguous), K-dim = 128 keys in 8 MMAs,
+      // issued as two batches of 64 keys: the softmax releases P in halves.
+      // A half of P is 32 tensor-memory columns (bf16 pairs); 64 keys of V
+      // are 64 rows of the V tile.
+      constexpr uint32_t kVStep16 = (16 * C::SW) >> 4;
+      auto issue_pv_half = [&](int t, uint32_t stg, int half, bool first) {
+        const uint32_t b = dv_lo + stg * kTile16 + half * 4 * kVStep16;
+        const uint32_t a_tmem = tmem + (t ? C::COL_S1 : C::COL_S0) + half * 32;
         const uint32_t d = tmem + (t ? C::COL_O1 : C::COL_O0);
-        ptx::mma_ts_x8_el<((16 * C::SW) >> 4)>(d, a_tmem, b, dv_hi, IDESC_PV, first ? 0u : 1u);
+        ptx::mma_ts_x4_el<kVStep16>(d, a_tmem, b, dv_hi, IDESC_PV, first ? 0u : 1u);
+      };
+      // Waits for each half of P_t, then issues its MMAs.
+      auto issue_pv = [&](int t, uint32_t stg, bool first, uint32_t parity) -> bool {
+        if (!bounded_wait_warp(ptx::smem_u32(&bars->p_half[t]), parity, bars, p.timeout_ns))
+          return false;
+        ptx::tc_fence_after_sync();
+        issue_pv_half(t, stg, 0, first);
+        if (!bounded_wait_warp(ptx::smem_u32(&bars->p_ready[t]), parity, bars, p.timeout_ns))
+          return false;
+        ptx::tc_fence_after_sync();
+        issue_pv_half(t, stg, 1, false);
+        return true;
       };
       // Wait until the ring's current stage is full; returns that stage.
       auto take_stage = [&](uint32_t& stg) -> bool {
@@ -462,11 +479,9 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
           if (!ok) break;
           const bool has_next = j + 1 < nkv;
           // O0 += P0 V_j
-          ok = bounded_wait_warp(ptx::smem_u32(&bars->p_ready[0]), pc0 & 1, bars, p.timeout_ns);
+          ok = issue_pv(0, sV, j == 0, pc0 & 1);
           if (!ok) break;
           ++pc0;
-          ptx::tc_fence_after_sync();
-          issue_pv(0, sV, j == 0);
           if (!has_next) ptx::mma_commit_el(ptx::smem_u32(&bars->o_full[0]));
           // S0 for key block j+1 as soon as P0 has been consumed.
           if (has_next) {
@@ -476,11 +491,9 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
             ptx::mma_commit_el(ptx::smem_u32(&bars->s_full[0]));
           }
           if (has1) {
-            ok = bounded_wait_warp(ptx::smem_u32(&bars->p_ready[1]), pc1 & 1, bars, p.timeout_ns);
+            ok = issue_pv(1, sV, j == 0, pc1 & 1);
             if (!ok) break;
             ++pc1;
-            ptx::tc_fence_after_sync();
-            issue_pv(1, sV, j == 0);
             if (!has_next) ptx::mma_commit_el(ptx::smem_u32(&bars->o_full[1]));
           }
           ptx::mma_commit_el(ptx::smem_u32(&bars->kv_empty[sV]));
@@ -518,6 +531,7 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
     const uint32_t tS = tmem + lane_base + (t ? C::COL_S1 : C::COL_S0);
     const uint32_t tO = tmem + lane_base + (t ? C::COL_O1 : C::COL_O0);
     const uint32_t bar_s = ptx::smem_u32(&bars->s_full[t]);
+    const uint32_t bar_ph = ptx::smem_u32(&bars->p_half[t]);
     const uint32_t bar_p = ptx::smem_u32(&bars->p_ready[t]);
     const uint32_t bar_o = ptx::smem_u32(&bars->o_full[t]);
     const float scale_log2 = p.scale_log2;
@@ -612,6 +626,17 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
         }
         const float m_use = (m == -INFINITY) ? 0.f : m;
         l *= alpha;
+        // P in two halves of 64 keys, each released as soon as it is in
+        // tensor memory so the first P·V MMAs overlap the second half's exp2.
+        // When O must be rescaled (rare: the max grew past the threshold) the
+        // first half waits until all of P is stored, so that the rescale runs
+        // with the scores already consumed.
+        const bool rescale_o = j > 0 && __any_sync(0xffffffffu, grow);
+        auto release = [&](int h) {
+          ptx::tmem_wait_st();
+          ptx::tc_fence_before_sync();
+          ptx::mbar_arrive(h ? bar_p : bar_ph);
+        };
         float2 lsum = make_float2(0.f, 0.f);
         if (!general) {
           const float2 sc2 = make_float2(sl2, sl2);
@@ -633,6 +658,7 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
               packed[c / 2] = ptx::pack_bf16x2(pr.x, pr.y);
             }
             ptx::tmem_st32x32b_x16(tS + cb / 2, packed);
+            if (cb == 32 && !rescale_o) release(0);
           }
         } else {
 #pragma unroll
@@ -646,12 +672,13 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
               packed[c / 2] = ptx::pack_bf16x2(p0, p1);
             }
             ptx::tmem_st32x32b_x16(tS + cb / 2, packed);
+            if (cb == 32 && !rescale_o) release(0);
           }
         }
         l += lsum.x + lsum.y;
-        // Rescale the accumulator O (after P(j-1)·V has landed: the S commit
-        // that released this iteration follows that MMA).
-        if (j > 0 && __any_sync(0xffffffffu, grow)) {
+        if (rescale_o) {
+          // P(j-1)·V has landed: the S commit that released this iteration
+          // follows it.
 #pragma unroll
           for (int cb = 0; cb < D; cb += 32) {
             uint32_t r[32];
@@ -660,10 +687,9 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
             for (int c = 0; c < 32; ++c) r[c] = __float_as_uint(__uint_as_float(r[c]) * alpha);
             ptx::tmem_st32x32b_x32(tO + cb, r);
           }
+          release(0);
         }
-        ptx::tmem_wait_st();
-        ptx::tc_fence_before_sync();
-        ptx::mbar_arrive(bar_p);
+        release(1);
       }
       if (!ok) break;
 
