@@ -119,3 +119,13 @@ def test_mask_validation():
                            ctypes.byref(mk), 0, out.data_ptr(), lse.data_ptr(), 1, 2, 64, 64, 64,
                            ctypes.c_float(0.125), None)
         assert rc == 1, (kind, data, heads)
+
+
+def test_causal_last_wave_single_tile_units():
+    """Causal with pair units = SMs + 10: the last wave runs single-tile units,
+    whose causal key limit is their own last row."""
+    G = torch.cuda.get_device_properties(0).multi_processor_count
+    inp = _inputs(64, 1, G // 2 + 5, 512, 512)
+    out, lse = _run(inp, causal=True)
+    o_ref, l_ref = _oracle(inp, causal=True)
+    compare(out, lse, o_ref, l_ref, label="causal last-wave singles")

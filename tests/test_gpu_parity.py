@@ -133,3 +133,28 @@ def test_invalid_arguments_launch_nothing():
     assert st(q=q.data_ptr() + 2) == 1
     torch.cuda.synchronize()
     assert torch.all(out == 7.0) and torch.all(lse == 7.0)
+
+
+def _sm_count():
+    return torch.cuda.get_device_properties(0).multi_processor_count
+
+
+@pytest.mark.parametrize("D,Nk", [(64, 300), (128, 129)])
+def test_last_wave_single_tile_units(D, Nk):
+    """Pair units = SMs + 8: the last wave's 8 pairs run as 16 single-tile units."""
+    G = _sm_count()
+    base = {64: "sd_self", 128: "flux_1024"}[D]
+    inp = workloads.make_inputs(base, device="cuda", B=1, H=G + 8, Nq=256, Nk=Nk)
+    out, lse = run_gpu(inp)
+    o_ref, lse_ref = run_oracle(inp)
+    compare(out, lse, o_ref, lse_ref, label=f"last-wave singles D{D} Nk{Nk}")
+
+
+def test_last_wave_single_tile_units_two_pairs_per_head():
+    """Two pair units per head (Nq 512): the split pairs span the last heads' halves."""
+    G = _sm_count()
+    H = G // 2 + 5                     # pairs = G + 10, R = 10
+    inp = workloads.make_inputs("sd_self", device="cuda", B=1, H=H, Nq=512, Nk=200)
+    out, lse = run_gpu(inp)
+    o_ref, lse_ref = run_oracle(inp)
+    compare(out, lse, o_ref, lse_ref, label="last-wave singles Nq512")

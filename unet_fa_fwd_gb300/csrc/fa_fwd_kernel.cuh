@@ -126,28 +126,44 @@ struct Params {  // 64-byte aligned through its CUtensorMap members
   int qtiles;             // ceil(Nq/128)
   unsigned long long timeout_ns;
   int inject_stall;    // test hook: CTA 0's producer withholds its 4th K/V tile
+  int tail_start;      // units >= tail_start are single query tiles (halves of the
+                       // last pair units; unsplit launches only), else == num_units
 };
 
-// One work unit: 256 query rows of one (b, h) against one range of key blocks.
+// One work unit: nq query tiles (256 rows, or 128 at the Nq tail and in the
+// last wave) of one (b, h) against one range of key blocks.
 struct Unit {
-  int bh, q0, split, tile0, ntiles;
+  int bh, q0, nq, split, tile0, ntiles;
 };
 
 // Units are numbered head-major, then query pair, then key range, so CTAs
-// running together share a head's K/V (and Q) in L2.
+// running together share a head's K/V (and Q) in L2.  When the pair units do
+// not fill the last wave of the persistent grid, the last ones are split into
+// single-tile units (two per pair, numbered from tail_start) so that wave is
+// shorter.
 __device__ __forceinline__ Unit decode_unit(const Params& p, int u) {
   Unit r;
-  r.split = u % p.num_splits;
-  const int rest = u / p.num_splits;
-  r.bh = rest / p.units_per_bh;
-  r.q0 = (rest % p.units_per_bh) * 256;
+  if (u >= p.tail_start) {
+    const int v = u - p.tail_start;
+    const int pair = p.tail_start + (v >> 1);  // unsplit launch: unit == pair index
+    r.split = 0;
+    r.bh = pair / p.units_per_bh;
+    r.q0 = (pair % p.units_per_bh) * 256 + (v & 1) * 128;
+    r.nq = 1;
+  } else {
+    r.split = u % p.num_splits;
+    const int rest = u / p.num_splits;
+    r.bh = rest / p.units_per_bh;
+    r.q0 = (rest % p.units_per_bh) * 256;
+    r.nq = (r.q0 + 128 < p.Nq) ? 2 : 1;
+  }
   // Balanced ranges: range s covers key blocks [s*nkv/S, (s+1)*nkv/S).
   r.tile0 = (int)((long long)r.split * p.nkv / p.num_splits);
   r.ntiles = (int)((long long)(r.split + 1) * p.nkv / p.num_splits) - r.tile0;
   if (p.causal) {
     // Key blocks past the unit's last query row are fully masked: skip them
     // (causal launches use one key range, so at least one block remains).
-    const int last_row = min(r.q0 + 255, p.Nq - 1);
+    const int last_row = min(r.q0 + 128 * r.nq - 1, p.Nq - 1);
     r.ntiles = min(r.ntiles, last_row / 128 + 1 - r.tile0);
   }
   return r;
@@ -315,7 +331,7 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
       for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uc) {
         const Unit un = decode_unit(p, u);
         const int bh = un.bh, q0 = un.q0;
-        const int ntiles = (q0 + 128 < p.Nq) ? 2 : 1;
+        const int ntiles = un.nq;
         ok = bounded_wait(ptx::smem_u32(&bars->q_empty), (uc & 1) ^ 1, bars, p.timeout_ns);
         if (!ok) break;
         const uint32_t qbar = ptx::smem_u32(&bars->q_full);
@@ -456,7 +472,7 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
 
       for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uc) {
         const Unit un = decode_unit(p, u);
-        const bool has1 = un.q0 + 128 < p.Nq;
+        const bool has1 = un.nq == 2;
         const int nkv = un.ntiles;
         ok = bounded_wait_warp(ptx::smem_u32(&bars->q_full), uc & 1, bars, p.timeout_ns);
         if (!ok) break;
@@ -543,7 +559,7 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
     for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
       const Unit un = decode_unit(p, u);
       const int bh = un.bh, q0 = un.q0;
-      if (t == 1 && !(q0 + 128 < p.Nq)) continue;
+      if (t == 1 && un.nq < 2) continue;
       const int qrow = q0 + t * 128 + row;
       const float* mask_b = p.mask ? p.mask + (size_t)(bh / p.H) * p.Nk : nullptr;
       const bool any_full_mask = p.full_mask != nullptr;  // warp-uniform
