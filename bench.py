@@ -383,6 +383,17 @@ def bench_native(args, world, rank, local):
 
     peaks, peak_src = read_peaks()
     peak = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS))
+    peak_sustained = peaks.get("bf16_tflops_sustained")
+
+    # ---- secondary bound: one exponential per score on the MUFU pipe ----
+    clock_summary = clocks.summary()
+    ex2_rate = fa.measure_ex2_rate(stream)
+    sm_count = torch.cuda.get_device_properties(device).multi_processor_count
+    clk_mhz = clock_summary.get("sm_mhz") or float(peaks.get("sm_max_mhz", 2070.0))
+    exps = float(B) * H * Nq * Nk
+    secondary = {"bound": "mufu_ex2", "ex2_per_clk_per_sm": round(ex2_rate, 2),
+                 "sm_mhz": clk_mhz, "exp_bound_ms": round(exps / (ex2_rate * sm_count * clk_mhz * 1e6) * 1e3, 4),
+                 "tensor_bound_ms": round(flops / (peak * 1e12) * 1e3, 4)}
     for v_ in also.values():
         if "tflops" in v_:
             v_["frac_of_peak"] = round(v_["tflops"] / peak, 4)
@@ -414,7 +425,7 @@ def bench_native(args, world, rank, local):
                        "masked": mask is not None, "parallelism": f"replicas{world}",
                        "l2": f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB of Q/K/V per step)"},
             "pct_of_peak": round(100.0 * kernel_tflops / peak, 2),
-            "clocks": clocks.summary(),
+            "clocks": clock_summary,
             "e2e": {"value": round(e2e_tflops, 2), "unit": "TFLOP/s",
                     "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": out_bytes,
                     "steps": e2e_steps, "overlap": "double-buffered: upload i+1 / download i-1 "
@@ -424,6 +435,9 @@ def bench_native(args, world, rank, local):
                          "unit": "TFLOP/s", "frac": round(kernel_tflops / peak, 4),
                          "traffic": read_traffic(args.workload),
                          "peak_source": f"{peak_src} bf16_tflops (burst; kernel timed alone)",
+                         "frac_of_sustained": (round(kernel_tflops / float(peak_sustained), 4)
+                                               if peak_sustained else None),
+                         "secondary": secondary,
                          "algorithmic_flops_per_launch": flops,
                          "algorithmic_bytes_per_launch": accounting.algorithmic_bytes(
                              B, H, Nq, Nk, D, masked=mask is not None)},

@@ -245,6 +245,22 @@ int fa_fwd_split_noalloc(const void* q, const void* k, const void* v, const floa
  */
 int fa_read_device_status(void* stream, int* status);
 
+/*
+ * fa_measure_ex2_rate — throughput of the exponential the forward takes once
+ * per score (ex2.approx.ftz.f32 on the special-function unit): runs a short
+ * probe kernel on `stream` (4 CTAs of 256 threads per SM, 16 independent
+ * chains per thread, each CTA timed with clock64) and writes the exponentials
+ * one SM completes per SM clock, bounded by its slowest CTA, to
+ * *ex2_per_clock_per_sm.  The exp-bound time of a launch is then
+ * B·H·Nq·Nk / (rate · SMs · clock).  ("算子加速：注意力、编译与融合",
+ * section "注意力：从O(N²)显存到分块": one exponential per score in the
+ * softmax.)  Diagnostic, blocking: synchronises `stream`.  Uses static device
+ * storage of the library; allocates nothing.  Returns FA_OK,
+ * FA_ERR_INVALID_ARGUMENT (NULL output), FA_ERR_UNSUPPORTED (more than 1024
+ * SMs) or FA_ERR_CUDA.
+ */
+int fa_measure_ex2_rate(void* stream, double* ex2_per_clock_per_sm);
+
 /* Human-readable name of a status code (static storage; never NULL). */
 const char* fa_status_string(int status);
 

@@ -30,7 +30,8 @@ def lib():
 
 def test_exports_every_declared_symbol(lib):
     names = _declared()
-    assert {"fa_fwd", "fa_status_string", "fa_version", "fa_read_device_status"} <= set(names)
+    assert {"fa_fwd", "fa_status_string", "fa_version", "fa_read_device_status",
+            "fa_measure_ex2_rate"} <= set(names)
     raw = ctypes.CDLL(_build.LIB)
     for n in names:
         assert hasattr(raw, n), n
@@ -160,3 +161,7 @@ def test_fp8_validation_before_any_cuda_call(lib):
     assert call(ws_bytes=need - 1) == 1
     assert call(D=48) == 2
     assert call(q=None) == 1
+
+
+def test_ex2_probe_validation_before_any_cuda_call(lib):
+    assert lib.fa_measure_ex2_rate(None, None) == 1   # FA_ERR_INVALID_ARGUMENT

@@ -75,6 +75,8 @@ def load_library() -> ctypes.CDLL:
             lib.fa_split_count.restype = i32
             lib.fa_read_device_status.argtypes = [vp, ctypes.POINTER(i32)]
             lib.fa_read_device_status.restype = i32
+            lib.fa_measure_ex2_rate.argtypes = [vp, ctypes.POINTER(ctypes.c_double)]
+            lib.fa_measure_ex2_rate.restype = i32
             lib.fa_status_string.argtypes = [i32]
             lib.fa_status_string.restype = ctypes.c_char_p
             lib.fa_version.argtypes = []
@@ -330,6 +332,15 @@ def fwd_split(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, mask: torch.Ten
                      device=q.device)
     fa_fwd_split(q, k, v, mask, out, lse, num_splits, ws, scale=scale, stream=stream)
     return out, lse
+
+
+def measure_ex2_rate(stream=None) -> float:
+    """Exponentials (ex2.approx.ftz.f32) one SM completes per SM clock, measured on the device."""
+    rate = ctypes.c_double(0.0)
+    rc = load_library().fa_measure_ex2_rate(_stream_handle(stream), ctypes.byref(rate))
+    if rc != FA_OK:
+        raise RuntimeError(f"fa_measure_ex2_rate failed: {status_string(rc)}")
+    return rate.value
 
 
 def read_device_status(stream=None) -> int:

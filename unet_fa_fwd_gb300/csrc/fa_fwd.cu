@@ -21,6 +21,7 @@
 #include "fa_fwd_kernel.cuh"
 #include "fa_quant.cuh"
 #include "fa_window.cuh"
+#include "fa_diag.cuh"
 
 namespace {
 
@@ -554,6 +555,31 @@ int fa_read_device_status(void* stream, int* status) {
     return FA_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return FA_ERR_CUDA;
   *status = value;
+  return FA_OK;
+}
+
+int fa_measure_ex2_rate(void* stream, double* ex2_per_clock_per_sm) {
+  if (!ex2_per_clock_per_sm) return FA_ERR_INVALID_ARGUMENT;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return FA_ERR_CUDA;
+  const int ctas = sms * fa::kDiagCtasPerSm;
+  if (ctas > fa::kDiagMaxCtas) return FA_ERR_UNSUPPORTED;
+  const int iters = 2048;
+  long long clk[fa::kDiagMaxCtas];
+  for (int rep = 0; rep < 2; ++rep)  // the first launch warms up clocks and caches
+    fa::fa_ex2_rate_kernel<<<ctas, fa::kDiagThreads, 0, s>>>(iters);
+  if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+  if (cudaMemcpyFromSymbolAsync(clk, fa::g_diag_clk, sizeof(long long) * ctas, 0,
+                                cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return FA_ERR_CUDA;
+  long long slowest = 1;
+  for (int b = 0; b < ctas; ++b) slowest = clk[b] > slowest ? clk[b] : slowest;
+  const double per_sm = (double)fa::kDiagCtasPerSm * fa::kDiagThreads * fa::kDiagChains * iters;
+  *ex2_per_clock_per_sm = per_sm / (double)slowest;
   return FA_OK;
 }
 
