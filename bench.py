@@ -229,18 +229,23 @@ def bench_native(args, world, rank, local):
 
     # ---- device-resident timed region ----
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    step_ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     with ClockSampler(local) as clocks:
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize(device)
         e0.record(stream)
-        for _ in range(args.steps):
+        for i in range(args.steps):
             step()
+            step_ev[i].record(stream)
         e1.record(stream)
         torch.cuda.synchronize(device)
         if world > 1:
             dist.barrier()
     secs = e0.elapsed_time(e1) / 1e3
+    # per-step device times (an event after every launch; the first pairs with e0)
+    step_ms = [e0.elapsed_time(step_ev[0])] + [step_ev[i - 1].elapsed_time(step_ev[i])
+                                               for i in range(1, args.steps)]
     max_secs = max_over_ranks(secs, device=device)
     if fa.read_device_status(stream) != 0:
         raise RuntimeError("kernel wait timed out in the timed region")
@@ -332,6 +337,41 @@ def bench_native(args, world, rank, local):
                                 "steps": n_h}
         del hw, hoAll, hl
 
+    # ---- the page's smaller configurations, each launch timed alone after an L2 flush ----
+    if args.also and rank == 0:
+        flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=device)  # > 129 MB L2
+        hbm = float(read_peaks()[0].get("hbm_gbs", 6671.5))
+        small = {}
+        for name in ("page_example", "sd_self", "sd_cross", "flux_1024"):
+            w_in = workloads.make_inputs(name, device=device)
+            sB, sH, sNq, sNk, sD = w_in["shape"]
+            so_ = torch.empty_like(w_in["q"])
+            sl_ = torch.empty((sB, sH, sNq), dtype=torch.float32, device=device)
+            call = lambda: fa.fa_fwd(w_in["q"], w_in["k"], w_in["v"], w_in["mask"], so_, sl_,
+                                     scale=w_in["scale"], stream=stream)
+            for _ in range(3):
+                call()
+            times = []
+            for _ in range(30):
+                flush.zero_()
+                c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                c0.record(stream)
+                call()
+                c1.record(stream)
+                torch.cuda.synchronize(device)
+                times.append(c0.elapsed_time(c1))
+            med = statistics.median(times)
+            sfl = accounting.attention_flops(sB, sH, sNq, sNk, sD)
+            sby = accounting.algorithmic_bytes(sB, sH, sNq, sNk, sD, masked=w_in["mask"] is not None)
+            small[name] = {"ms_median": round(med, 4), "ms_min": round(min(times), 4),
+                           "ms_max": round(max(times), 4), "tflops": round(sfl / med / 1e9, 1),
+                           "hbm_gbs": round(sby / med / 1e6, 1),
+                           "hbm_frac": round(sby / med / 1e6 / hbm, 4)}
+            del w_in, so_, sl_
+        also["small_configs"] = {"l2": "flushed (256 MB write) before every timed launch",
+                                 "launches": 30, "configs": small}
+        del flush
+
     # ---- FP8 (e4m3 Q K^T) forward on the same workload, pre-pass included ----
     if args.also and rank == 0:
         ws8 = torch.empty(fa.fp8_workspace_bytes(B, H, Nq, Nk, D), dtype=torch.uint8, device=device)
@@ -405,7 +445,8 @@ def bench_native(args, world, rank, local):
         cpu = {"value": cflops / csecs / 1e12, "unit": "TFLOP/s", "cores": sampler.threads,
                "kind": "oracle",
                "sample": f"{rows} seeded query rows per head x {B * H} heads of {args.workload} "
-                         f"(all {Nk} keys), fp64 C oracle, {csecs:.1f} s"}
+                         f"(all {Nk} keys), fp64 C oracle, {csecs:.1f} s",
+               "extrapolated_full_s": round(csecs * Nq / rows, 1)}
 
     if rank == 0:
         line = {
@@ -425,6 +466,8 @@ def bench_native(args, world, rank, local):
                        "masked": mask is not None, "parallelism": f"replicas{world}",
                        "l2": f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB of Q/K/V per step)"},
             "pct_of_peak": round(100.0 * kernel_tflops / peak, 2),
+            "step_ms": {"median": round(statistics.median(step_ms), 4),
+                        "min": round(min(step_ms), 4), "max": round(max(step_ms), 4)},
             "clocks": clock_summary,
             "e2e": {"value": round(e2e_tflops, 2), "unit": "TFLOP/s",
                     "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": out_bytes,
@@ -439,6 +482,8 @@ def bench_native(args, world, rank, local):
                                                if peak_sustained else None),
                          "secondary": secondary,
                          "algorithmic_flops_per_launch": flops,
+                         "hbm_gbs": round(accounting.algorithmic_bytes(
+                             B, H, Nq, Nk, D, masked=mask is not None) / (ms_per_step * 1e6), 1),
                          "algorithmic_bytes_per_launch": accounting.algorithmic_bytes(
                              B, H, Nq, Nk, D, masked=mask is not None)},
             "cpu_baseline": cpu,
