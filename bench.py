@@ -41,6 +41,8 @@ def kernel_source_hash() -> str:
     from unet_fa_fwd_gb300 import _build
     h = hashlib.sha256()
     for path in _build.sources():
+        if not path.endswith((".cu", ".cuh", ".inc", ".h")):
+            continue  # generators and notes are not compiled
         with open(path, "rb") as f:
             h.update(os.path.basename(path).encode())
             h.update(f.read())
