@@ -374,6 +374,65 @@ def bench_native(args, world, rank, local):
                                  "launches": 30, "configs": small}
         del flush
 
+    # ---- causal, a general additive mask and window attention (warm, back to back) ----
+    def time_call(fn, n):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize(device)
+        t0_, t1_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0_.record(stream)
+        for _ in range(n):
+            fn()
+        t1_.record(stream)
+        torch.cuda.synchronize(device)
+        if fa.read_device_status(stream) != 0:
+            raise RuntimeError("kernel wait timed out")
+        return t0_.elapsed_time(t1_) / n
+
+    if args.also and rank == 0:
+        ext = {}
+        # causal at the benchmark shape: the useful FLOPs count keys j <= i only
+        oc_, lc_ = torch.empty_like(q), torch.empty_like(lse)
+        msc = time_call(lambda: fa.fa_fwd_ex(q, k, v, oc_, lc_, causal=True, scale=inp["scale"],
+                                             stream=stream), max(5, args.steps // 10))
+        kept = (Nq * (Nq + 1) // 2 if Nq <= Nk          # sum over rows i of min(i + 1, Nk)
+                else Nk * (Nk + 1) // 2 + (Nq - Nk) * Nk)
+        cfl = 4.0 * B * H * D * kept
+        ext["causal"] = {"workload": args.workload, "ms_per_step": round(msc, 4),
+                         "tflops_useful": round(cfl / msc / 1e9, 1),
+                         "note": "FLOPs of the unmasked (j <= i) pairs only"}
+        del oc_, lc_
+        # additive fp32 mask [B, 1, Nq, Nk] (broadcast over heads) at FLUX 1024^2
+        wm = workloads.make_inputs("flux_1024", device=device)
+        mB, mH, mNq, mNk, mD = wm["shape"]
+        g = torch.Generator(device=device).manual_seed(2024)
+        fmask = torch.randn((mB, 1, mNq, mNk), generator=g, device=device, dtype=torch.float32)
+        om_ = torch.empty_like(wm["q"])
+        lm_ = torch.empty((mB, mH, mNq), dtype=torch.float32, device=device)
+        msm = time_call(lambda: fa.fa_fwd_ex(wm["q"], wm["k"], wm["v"], om_, lm_, full_mask=fmask,
+                                             scale=wm["scale"], stream=stream), 20)
+        ext["additive_mask"] = {"workload": "flux_1024", "mask": "fp32 [B,1,Nq,Nk] N(0,1)",
+                                "ms_per_step": round(msm, 4),
+                                "tflops": round(accounting.attention_flops(mB, mH, mNq, mNk, mD)
+                                                / msm / 1e9, 1),
+                                "mask_mb": round(fmask.numel() * 4 / 1e6, 1)}
+        del wm, fmask, om_, lm_
+        # window / shifted-window attention on the SD 512^2 latent grid (64 x 64 tokens)
+        ww = workloads.make_inputs("sd_self", device=device)
+        wB, wH, wN, _, wD = ww["shape"]
+        win = {}
+        for (wh, wwid, sh) in ((8, 8, 0), (8, 8, 4), (16, 16, 8)):
+            msw = time_call(lambda: fa.fwd_window(ww["q"], ww["k"], ww["v"], 64, 64, wh, wwid, sh,
+                                                  sh, scale=ww["scale"], stream=stream), 20)
+            wfl = 4.0 * wB * wH * wN * (wh * wwid) * wD
+            win[f"{wh}x{wwid}_shift{sh}"] = {"ms_per_step": round(msw, 4),
+                                            "tflops": round(wfl / msw / 1e9, 1)}
+        ext["window"] = {"workload": "sd_self grid 64x64, B2 H8 D64",
+                         "note": "gather + attention + scatter kernels, outputs allocated by the "
+                                 "binding", "configs": win}
+        del ww
+        also["masks_causal_window"] = ext
+
     # ---- FP8 (e4m3 Q K^T) forward on the same workload, pre-pass included ----
     if args.also and rank == 0:
         ws8 = torch.empty(fa.fp8_workspace_bytes(B, H, Nq, Nk, D), dtype=torch.uint8, device=device)

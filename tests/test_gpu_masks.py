@@ -52,8 +52,10 @@ def test_causal(D, Nq, Nk):
 
 @pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("heads", [1, 2])
-@pytest.mark.parametrize("Nq,Nk", [(130, 200), (256, 384)])
+@pytest.mark.parametrize("Nq,Nk", [(130, 200), (256, 384), (200, 301)])
 def test_additive_full_mask(D, heads, Nq, Nk):
+    """Nk 200 / 384: 16-byte mask loads (8 keys at a time) with a ragged last
+    block; Nk 301: rows not 16-byte aligned, scalar loads."""
     inp = _inputs(D, 2, 2, Nq, Nk)
     g = torch.Generator(device="cuda").manual_seed(5)
     m = torch.randn(2, heads, Nq, Nk, generator=g, device="cuda") * 2
@@ -66,15 +68,17 @@ def test_additive_full_mask(D, heads, Nq, Nk):
 
 @pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("causal", [False, True])
-def test_bool_mask(D, causal):
-    inp = _inputs(D, 1, 3, 200, 333)
+@pytest.mark.parametrize("Nk", [333, 336, 332])
+def test_bool_mask(D, causal, Nk):
+    """Nk 336: 8-byte mask loads; 333 and 332: rows not 8-byte aligned, scalar loads."""
+    inp = _inputs(D, 1, 3, 200, Nk)
     g = torch.Generator(device="cuda").manual_seed(6)
-    keep = torch.rand(1, 3, 200, 333, generator=g, device="cuda") > 0.4
+    keep = torch.rand(1, 3, 200, Nk, generator=g, device="cuda") > 0.4
     keep[..., 0] = True
     out, lse = _run(inp, full_mask=keep.contiguous(), causal=causal)
     add = torch.where(keep, 0.0, float("-inf")).float()
     o_ref, l_ref = _oracle(inp, full_mask=add, causal=causal)
-    compare(out, lse, o_ref, l_ref, label=f"bool D{D} causal{causal}")
+    compare(out, lse, o_ref, l_ref, label=f"bool D{D} causal{causal} Nk{Nk}")
 
 
 def test_key_padding_through_ex_matches_fa_fwd():

@@ -58,7 +58,7 @@ def test_small_shapes_and_tails(D, Nq, Nk):
 
 
 @pytest.mark.parametrize("D", [32, 64, 128])
-@pytest.mark.parametrize("Nk", [80, 200, 640])
+@pytest.mark.parametrize("Nk", [80, 200, 640, 77])
 def test_key_padding_mask(D, Nk):
     inp = workloads.make_inputs("sd_cross", device="cuda", B=3, H=2, Nq=333, Nk=Nk)
     # widen the head dim by rebuilding q/k/v with the requested D

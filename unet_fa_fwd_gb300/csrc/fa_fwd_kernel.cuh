@@ -150,6 +150,15 @@ __device__ __forceinline__ Unit decode_unit(const Params& p, int u) {
     r.bh = pair / p.units_per_bh;
     r.q0 = (pair % p.units_per_bh) * 256 + (v & 1) * 128;
     r.nq = 1;
+  } else if (p.causal) {
+    // Causal (one key range): a pair's work grows with its query position, so
+    // units run heaviest first across all heads (pair index descending, heads
+    // inner); with the round-robin assignment this keeps the CTAs' totals
+    // within a few percent, and the units of a head still start together.
+    r.split = 0;
+    r.bh = u % p.BH;
+    r.q0 = (p.units_per_bh - 1 - u / p.BH) * 256;
+    r.nq = (r.q0 + 128 < p.Nq) ? 2 : 1;
   } else {
     r.split = u % p.num_splits;
     const int rest = u / p.num_splits;
@@ -616,18 +625,57 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
             else
               fmask_f = static_cast<const float*>(p.full_mask) + fm_row * p.Nk;
           }
+          // Masks are read 8 keys at a time: two 16-byte loads of fp32, one
+          // 8-byte load of uint8, when the 8 keys lie inside Nk and the row
+          // start is aligned (Nk a multiple of 4 / 8); scalar loads otherwise.
+          const bool vec_f = (p.Nk & 3) == 0, vec_b = (p.Nk & 7) == 0;
 #pragma unroll
-          for (int c = 0; c < 128; ++c) {
-            const int key = kbase + c;
-            float tv = -INFINITY;
-            if (key < p.Nk && !(p.causal && key > qrow)) {
-              tv = s[c] * sl2;
-              if (mask_b) tv = fmaf(__ldg(mask_b + key), kLog2e, tv);
-              if (fmask_f) tv = fmaf(__ldg(fmask_f + key), kLog2e, tv);
-              if (fmask_b && __ldg(fmask_b + key) == 0) tv = -INFINITY;
+          for (int cb = 0; cb < 128; cb += 8) {
+            const int key0 = kbase + cb;
+            const bool whole = key0 + 8 <= p.Nk;
+            float add[8];
+            bool keep[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              add[i] = 0.f;
+              keep[i] = true;
             }
-            s[c] = tv;
-            mx = fmaxf(mx, tv);
+            const float* madd = mask_b ? mask_b : fmask_f;  // at most one additive mask
+            if (madd) {
+              if (whole && vec_f) {
+                const float4 a = __ldg(reinterpret_cast<const float4*>(madd + key0));
+                const float4 b = __ldg(reinterpret_cast<const float4*>(madd + key0 + 4));
+                add[0] = a.x; add[1] = a.y; add[2] = a.z; add[3] = a.w;
+                add[4] = b.x; add[5] = b.y; add[6] = b.z; add[7] = b.w;
+              } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                  if (key0 + i < p.Nk) add[i] = __ldg(madd + key0 + i);
+              }
+            }
+            if (fmask_b) {
+              if (whole && vec_b) {
+                const uint2 v = __ldg(reinterpret_cast<const uint2*>(fmask_b + key0));
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  keep[i] = ((v.x >> (8 * i)) & 0xffu) != 0u;
+                  keep[4 + i] = ((v.y >> (8 * i)) & 0xffu) != 0u;
+                }
+              } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                  if (key0 + i < p.Nk) keep[i] = __ldg(fmask_b + key0 + i) != 0;
+              }
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int key = key0 + i;
+              float tv = -INFINITY;
+              if (key < p.Nk && !(p.causal && key > qrow) && keep[i])
+                tv = fmaf(add[i], kLog2e, s[cb + i] * sl2);
+              s[cb + i] = tv;
+              mx = fmaxf(mx, tv);
+            }
           }
         }
         const float m_new = fmaxf(m, mx);
