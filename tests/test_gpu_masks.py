@@ -133,3 +133,27 @@ def test_causal_last_wave_single_tile_units():
     out, lse = _run(inp, causal=True)
     o_ref, l_ref = _oracle(inp, causal=True)
     compare(out, lse, o_ref, l_ref, label="causal last-wave singles")
+
+
+@pytest.mark.parametrize("kind", ["additive", "bool"])
+def test_mask_base_not_vector_aligned(kind):
+    """The C ABI admits an fp32 mask aligned to 4 bytes and a uint8 mask at any
+    address: such masks take the scalar load path (no misaligned vector loads)."""
+    Nq, Nk = 150, 256
+    inp = _inputs(64, 1, 2, Nq, Nk)
+    g = torch.Generator(device="cuda").manual_seed(9)
+    if kind == "additive":
+        buf = torch.empty(1 * 2 * Nq * Nk + 1, device="cuda", dtype=torch.float32)
+        m = buf[1:].view(1, 2, Nq, Nk)            # base 4 bytes past a 256-byte boundary
+        m.copy_(torch.randn(1, 2, Nq, Nk, generator=g, device="cuda"))
+        ref_mask = m.clone()
+    else:
+        buf = torch.empty(1 * 2 * Nq * Nk + 3, device="cuda", dtype=torch.bool)
+        m = buf[3:].view(1, 2, Nq, Nk)            # base 3 bytes past a 256-byte boundary
+        m.copy_(torch.rand(1, 2, Nq, Nk, generator=g, device="cuda") > 0.3)
+        m[..., 0] = True
+        ref_mask = torch.where(m, 0.0, float("-inf")).float()
+    assert m.data_ptr() % 16 != 0
+    out, lse = _run(inp, full_mask=m)
+    o_ref, l_ref = _oracle(inp, full_mask=ref_mask)
+    compare(out, lse, o_ref, l_ref, label=f"{kind} mask, unaligned base")

@@ -510,11 +510,19 @@ int fa_fwd_window(const void* q, const void* k, const void* v, void* out, float*
     return FA_ERR_INVALID_ARGUMENT;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse))
     return FA_ERR_INVALID_ARGUMENT;
-  fa::WindowGeom g{B, H, img_h, img_w, win_h, win_w, 0, 0, D};
+  fa::WindowGeom g{B, H, img_h, img_w, win_h, win_w, 0, 0, D, 1};
   g.shift_h = ((shift_h % img_h) + img_h) % img_h;
   g.shift_w = ((shift_w % img_w) + img_w) % img_w;
   const long long nw = g.windows();
   if ((long long)B * nw > INT_MAX) return FA_ERR_INVALID_ARGUMENT;
+  // Pack windows of up to 64 tokens, as many as fill a 128-row tile, into each
+  // batch entry (a divisor of the window count, so every entry is full).
+  const int Nw = g.win_tokens();
+  if (Nw <= 64) {
+    int pk = 128 / Nw;
+    while (pk > 1 && ((long long)B * nw) % pk) --pk;
+    g.pack = pk;
+  }
 
   char* ws = static_cast<char*>(workspace);
   const size_t t_al = align256(t_bytes);
@@ -534,8 +542,13 @@ int fa_fwd_window(const void* q, const void* k, const void* v, void* out, float*
       static_cast<const uint4*>(q), static_cast<const uint4*>(k), static_cast<const uint4*>(v),
       static_cast<uint4*>(qw), static_cast<uint4*>(kw), static_cast<uint4*>(vw), g, chunks);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
-  const int Nw = g.win_tokens();
-  int rc = fa_fwd(qw, kw, vw, nullptr, ow, lw, (int)(B * nw), H, Nw, Nw, D, scale, stream);
+  const int entries = (int)(B * nw / g.pack), Ne = g.entry_tokens();
+  fa::Params prm;
+  DeviceState* st = nullptr;
+  int rc = prepare(qw, kw, vw, nullptr, ow, lw, entries, H, Ne, Ne, D, scale, &prm, &st);
+  if (rc != FA_OK) return rc;
+  prm.seg = g.pack > 1 ? Nw : 0;  // each row sees its own window only
+  rc = launch_fwd(prm, *st, D, s);
   if (rc != FA_OK) return rc;
   fa::fa_window_scatter_kernel<<<(int)blocks, 256, 0, s>>>(
       static_cast<const uint4*>(ow), lw, static_cast<uint4*>(out), lse, g, chunks);

@@ -112,6 +112,8 @@ struct Params {  // 64-byte aligned through its CUtensorMap members
   int full_mask_bool;     // 0: additive fp32; 1: uint8, nonzero = keep, 0 = -inf
   int mask_heads;         // 1 (broadcast over heads) or H
   int causal;             // exclude key j > query i
+  int seg;                // > 0: rows and keys form consecutive segments of this length
+                          // and a row sees only keys of its own segment (packed windows)
   int H, Nq, Nk, BH;
   int num_units;       // BH * units_per_bh * num_splits
   int units_per_bh;    // ceil(ceil(Nq/128)/2)
@@ -599,7 +601,8 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
         // is taken on raw scores and scaled once.  Otherwise scores are
         // materialised in the log2 domain with the mask and the Nk tail.
         const bool general = (mask_b != nullptr) || any_full_mask || (kbase + 128 > p.Nk) ||
-                             !(sl2 >= 0.f) || (p.causal && kbase + 127 > tile_row0);
+                             !(sl2 >= 0.f) || (p.causal && kbase + 127 > tile_row0) ||
+                             p.seg > 0;
         float mx;
         if (!general) {
           float a0 = s[0], a1 = s[1], a2 = s[2], a3 = s[3];
@@ -626,9 +629,17 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
               fmask_f = static_cast<const float*>(p.full_mask) + fm_row * p.Nk;
           }
           // Masks are read 8 keys at a time: two 16-byte loads of fp32, one
-          // 8-byte load of uint8, when the 8 keys lie inside Nk and the row
-          // start is aligned (Nk a multiple of 4 / 8); scalar loads otherwise.
-          const bool vec_f = (p.Nk & 3) == 0, vec_b = (p.Nk & 7) == 0;
+          // 8-byte load of uint8, when the 8 keys lie inside Nk and every row
+          // start is aligned (base pointer aligned and Nk a multiple of 4 / 8;
+          // the C ABI admits 4-byte-aligned fp32 and unaligned uint8 masks);
+          // scalar loads otherwise.
+          // Keys of this row's segment (all keys when rows are not segmented).
+          const int seg_lo = p.seg > 0 ? (qrow / p.seg) * p.seg : 0;
+          const int seg_hi = p.seg > 0 ? seg_lo + p.seg : p.Nk;
+          const float* madd_base = p.mask ? p.mask : (p.full_mask_bool ? nullptr
+                                                      : static_cast<const float*>(p.full_mask));
+          const bool vec_f = (p.Nk & 3) == 0 && (reinterpret_cast<uintptr_t>(madd_base) & 15u) == 0;
+          const bool vec_b = (p.Nk & 7) == 0 && (reinterpret_cast<uintptr_t>(p.full_mask) & 7u) == 0;
 #pragma unroll
           for (int cb = 0; cb < 128; cb += 8) {
             const int key0 = kbase + cb;
@@ -671,7 +682,8 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
             for (int i = 0; i < 8; ++i) {
               const int key = key0 + i;
               float tv = -INFINITY;
-              if (key < p.Nk && !(p.causal && key > qrow) && keep[i])
+              if (key < p.Nk && !(p.causal && key > qrow) && keep[i] && key >= seg_lo &&
+                  key < seg_hi)
                 tv = fmaf(add[i], kLog2e, s[cb + i] * sl2);
               s[cb + i] = tv;
               mx = fmaxf(mx, tv);
