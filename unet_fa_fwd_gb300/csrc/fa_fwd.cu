@@ -279,11 +279,11 @@ void launch_quant(const void* q, const void* k, char* ws, const F8Layout& L, int
       reinterpret_cast<const float*>(ws + L.partial), reinterpret_cast<float*>(ws + L.mean), BH, D,
       kF8ColsumSplits, Nk);
   const int kt = (Nk + 127) / 128, qt = (Nq + 127) / 128;
-  fa::fa_quant_rows_kernel<D, true><<<BH * kt, 128, 0, s>>>(
+  fa::fa_quant_rows_kernel<D, true><<<BH * kt, 256, 0, s>>>(
       static_cast<const __nv_bfloat16*>(k), reinterpret_cast<const float*>(ws + L.mean),
       reinterpret_cast<uint8_t*>(ws + L.k8), reinterpret_cast<float*>(ws + L.k_scale), nullptr, Nk,
       kt, scale);
-  fa::fa_quant_rows_kernel<D, false><<<BH * qt, 128, 0, s>>>(
+  fa::fa_quant_rows_kernel<D, false><<<BH * qt, 256, 0, s>>>(
       static_cast<const __nv_bfloat16*>(q), reinterpret_cast<const float*>(ws + L.mean),
       reinterpret_cast<uint8_t*>(ws + L.q8), reinterpret_cast<float*>(ws + L.q_scale),
       reinterpret_cast<float*>(ws + L.corr), Nq, qt, scale);

@@ -23,26 +23,41 @@ namespace fa {
 constexpr float kE4M3Max = 448.f;
 
 // Partial per-channel sums of K: block (bh, split) sums tokens
-// [split*per, (split+1)*per) into partial[bh][split][D].  256 threads =
-// 256/D token lanes x D channels; coalesced along the channel.
+// [split*per, (split+1)*per) into partial[bh][split][D].  256 threads: thread
+// (r, part) reads the 16-byte chunk `part` (8 channels) of rows r, r + RL, ...,
+// so a warp's loads cover whole rows contiguously.
 template <int D>
 __global__ void __launch_bounds__(256) fa_k_colsum_kernel(const __nv_bfloat16* __restrict__ k,
                                                           float* __restrict__ partial, int Nk,
                                                           int nsplit) {
-  constexpr int LANES = 256 / D;
+  constexpr int PARTS = D / 8;          // 16-byte chunks per row
+  constexpr int RL = 256 / PARTS;       // rows read per step
   const int bh = blockIdx.x, sp = blockIdx.y;
   const int per = (Nk + nsplit - 1) / nsplit;
   const int t0 = sp * per, t1 = min(Nk, t0 + per);
-  const int c = threadIdx.x % D, r = threadIdx.x / D;
-  float acc = 0.f;
-  for (int t = t0 + r; t < t1; t += LANES) acc += __bfloat162float(k[((size_t)bh * Nk + t) * D + c]);
-  __shared__ float red[256];
-  red[threadIdx.x] = acc;
-  __syncthreads();
-  if (r == 0) {
-    float sum = 0.f;
+  const int part = threadIdx.x % PARTS, r = threadIdx.x / PARTS;
+  float acc[8];
 #pragma unroll
-    for (int i = 0; i < LANES; ++i) sum += red[i * D + c];
+  for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+  const uint4* base = reinterpret_cast<const uint4*>(k + (size_t)bh * Nk * D) + part;
+  for (int t = t0 + r; t < t1; t += RL) {
+    const uint4 u = __ldg(base + (size_t)t * PARTS);
+    const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = __bfloat1622float2(h2[e]);
+      acc[2 * e] += f.x;
+      acc[2 * e + 1] += f.y;
+    }
+  }
+  __shared__ float red[RL][D + 1];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) red[r][part * 8 + e] = acc[e];
+  __syncthreads();
+  for (int c = threadIdx.x; c < D; c += 256) {
+    float sum = 0.f;
+#pragma unroll 4
+    for (int i = 0; i < RL; ++i) sum += red[i][c];
     partial[((size_t)bh * nsplit + sp) * D + c] = sum;
   }
 }
@@ -57,70 +72,84 @@ __global__ void fa_k_mean_kernel(const float* __restrict__ partial, float* __res
   mean[i] = sum / (float)Nk;
 }
 
-// One CTA of 128 threads per (bh, 128-row block); thread r owns row blk*128+r.
+// One CTA of 256 threads per (bh, 128-row block).  The block's rows are read
+// as 16-byte chunks (8 elements), chunk i by thread i mod 256, so a warp's
+// loads and its 8-byte e4m3 stores cover whole rows contiguously.  The block
+// max goes through shared memory; the Q row dot with mean(K) (for lse_corr) is
+// reduced across the D/8 lanes holding one row.
 // IS_K: subtract the channel mean first.  Q: also write scale * (q_i . mean_k).
 template <int D, bool IS_K>
-__global__ void __launch_bounds__(128) fa_quant_rows_kernel(
+__global__ void __launch_bounds__(256) fa_quant_rows_kernel(
     const __nv_bfloat16* __restrict__ x, const float* __restrict__ mean_k, uint8_t* __restrict__ x8,
     float* __restrict__ block_scale, float* __restrict__ lse_corr, int N, int nblk, float scale) {
+  constexpr int PARTS = D / 8;                 // chunks per row (4, 8 or 16)
+  constexpr int PER = 128 * PARTS / 256;       // chunks per thread (2, 4 or 8)
   const int bh = blockIdx.x / nblk, blk = blockIdx.x % nblk;
-  const int r = threadIdx.x;
-  const int n = blk * 128 + r;
+  const int tid = threadIdx.x;
   __shared__ float smean[D];
-  __shared__ float wmax[4];
-  for (int c = r; c < D; c += 128) smean[c] = mean_k[(size_t)bh * D + c];
+  __shared__ float wmax[8];
+  for (int c = tid; c < D; c += 256) smean[c] = mean_k[(size_t)bh * D + c];
   __syncthreads();
 
-  float val[D];
-  float amax = 0.f, dot = 0.f;
-  if (n < N) {
-    const uint4* src = reinterpret_cast<const uint4*>(x + ((size_t)bh * N + n) * D);
+  const size_t row0 = (size_t)bh * N + (size_t)blk * 128;
+  const uint4* src = reinterpret_cast<const uint4*>(x + row0 * D);
+  float val[PER][8];
+  float amax = 0.f;
 #pragma unroll
-    for (int v = 0; v < D / 8; ++v) {
-      const uint4 u = __ldg(src + v);
-      const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&u);
+  for (int i = 0; i < PER; ++i) {
+    const int chunk = i * 256 + tid;
+    const int r = chunk / PARTS, part = chunk % PARTS;
+    const bool valid = blk * 128 + r < N;
+    uint4 u = make_uint4(0u, 0u, 0u, 0u);
+    if (valid) u = __ldg(src + chunk);
+    const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&u);
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 f = __bfloat1622float2(h2[e]);
-        const int c = v * 8 + e * 2;
-        val[c] = IS_K ? f.x - smean[c] : f.x;
-        val[c + 1] = IS_K ? f.y - smean[c + 1] : f.y;
-      }
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = __bfloat1622float2(h2[e]);
+      const int c = part * 8 + 2 * e;
+      val[i][2 * e] = (IS_K && valid) ? f.x - smean[c] : f.x;
+      val[i][2 * e + 1] = (IS_K && valid) ? f.y - smean[c + 1] : f.y;
     }
 #pragma unroll
-    for (int c = 0; c < D; ++c) {
-      amax = fmaxf(amax, fabsf(val[c]));
-      if (!IS_K) dot = fmaf(val[c], smean[c], dot);
+    for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(val[i][e]));
+    if (!IS_K) {
+      float dot = 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) dot = fmaf(val[i][e], smean[part * 8 + e], dot);
+#pragma unroll
+      for (int o = PARTS / 2; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+      if (part == 0 && valid) lse_corr[row0 + r] = scale * dot;
     }
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-  if ((r & 31) == 0) wmax[r >> 5] = amax;
+  if ((tid & 31) == 0) wmax[tid >> 5] = amax;
   __syncthreads();
-  amax = fmaxf(fmaxf(wmax[0], wmax[1]), fmaxf(wmax[2], wmax[3]));
+  amax = wmax[0];
+#pragma unroll
+  for (int w = 1; w < 8; ++w) amax = fmaxf(amax, wmax[w]);
   const float s = amax > 0.f ? amax / kE4M3Max : 1.f;
   const float inv = 1.f / s;
-  if (r == 0) block_scale[(size_t)bh * nblk + blk] = s;
-  if (n < N) {
-    uint4* dst = reinterpret_cast<uint4*>(x8 + ((size_t)bh * N + n) * D);
+  if (tid == 0) block_scale[(size_t)bh * nblk + blk] = s;
+  uint2* dst = reinterpret_cast<uint2*>(x8 + row0 * D);
 #pragma unroll
-    for (int v = 0; v < D / 16; ++v) {
-      uint32_t w[4];
+  for (int i = 0; i < PER; ++i) {
+    const int chunk = i * 256 + tid;
+    if (blk * 128 + chunk / PARTS >= N) continue;
+    uint32_t w[2];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        // element c + b goes to byte b (little-endian order of the row)
-        uint32_t word = 0;
+    for (int h = 0; h < 2; ++h) {
+      // element 4h + b of the chunk goes to byte b of word h (row order)
+      uint32_t word = 0;
 #pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          const __nv_fp8_storage_t q8 =
-              __nv_cvt_float_to_fp8(val[v * 16 + e * 4 + b] * inv, __NV_SATFINITE, __NV_E4M3);
-          word |= (uint32_t)q8 << (8 * b);
-        }
-        w[e] = word;
+      for (int b = 0; b < 4; ++b) {
+        const __nv_fp8_storage_t q8 =
+            __nv_cvt_float_to_fp8(val[i][4 * h + b] * inv, __NV_SATFINITE, __NV_E4M3);
+        word |= (uint32_t)q8 << (8 * b);
       }
-      dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
+      w[h] = word;
     }
-    if (!IS_K) lse_corr[(size_t)bh * N + n] = scale * dot;
+    dst[chunk] = make_uint2(w[0], w[1]);
   }
 }
 
