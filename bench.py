@@ -36,15 +36,17 @@ KERNEL_NAME = "fa_fwd_kernel"
 
 # --------------------------------------------------------------------- helpers
 
+KERNEL_FILES = ("fa_fwd_kernel.cuh", "sm100_ptx.cuh", "tmem_ldst.inc", "mma_batch.inc")
+
+
 def kernel_source_hash() -> str:
-    """sha256 over the CUDA sources and the C header (identifies a kernel build)."""
-    from unet_fa_fwd_gb300 import _build
+    """sha256 over the files that define the attention kernel and its launch plan
+    (device code, tensor-memory / MMA wrappers, unit schedule)."""
     h = hashlib.sha256()
-    for path in _build.sources():
-        if not path.endswith((".cu", ".cuh", ".inc", ".h")):
-            continue  # generators and notes are not compiled
-        with open(path, "rb") as f:
-            h.update(os.path.basename(path).encode())
+    csrc = os.path.join(ROOT, "unet_fa_fwd_gb300", "csrc")
+    for name in KERNEL_FILES:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
             h.update(f.read())
     return h.hexdigest()
 

@@ -201,23 +201,8 @@ int prepare(const void* q, const void* k, const void* v, const float* mask, void
 }
 
 int launch_fwd(const fa::Params& prm_in, DeviceState& st, int D, cudaStream_t s, bool f8 = false) {
-  // Last-wave balancing: with P pair units on G persistent CTAs, the final
-  // wave holds R = P mod G of them.  If R <= G/2, those R pairs run as 2R
-  // single-tile units instead, one per CTA, which finish sooner than pairs.
-  // Only for unsplit, non-causal launches whose heads have an even number of
-  // query tiles (every pair unit then holds two tiles; causal launches order
-  // their units heaviest first instead).
   fa::Params prm = prm_in;
-  prm.tail_start = prm.num_units;
-  const int G = st.sm_count;
-  if (prm.num_splits == 1 && !prm.causal && ((prm.Nq + 127) / 128) % 2 == 0 && prm.num_units > G &&
-      prm.num_units <= INT_MAX - G) {
-    const int R = prm.num_units % G;
-    if (R > 0 && 2 * R <= G) {
-      prm.tail_start = prm.num_units - R;
-      prm.num_units += R;
-    }
-  }
+  fa::plan_last_wave(prm, st.sm_count);
   if (f8) {
     switch (D) {
       case 32: return launch<32, true>(prm, st, 3, s);

@@ -28,6 +28,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <climits>
 #include <cstdint>
 
 #include "sm100_ptx.cuh"
@@ -178,6 +179,25 @@ __device__ __forceinline__ Unit decode_unit(const Params& p, int u) {
     r.ntiles = min(r.ntiles, last_row / 128 + 1 - r.tile0);
   }
   return r;
+}
+
+// Host side of the unit schedule, last-wave balancing: with P pair units on
+// G persistent CTAs, the final wave holds R = P mod G of them.  If R <= G/2,
+// those R pairs run as 2R single-tile units instead (numbered from
+// tail_start), one per CTA, which finish sooner than pairs.  Only for unsplit,
+// non-causal launches whose heads have an even number of query tiles (every
+// pair unit then holds two tiles; causal launches order their units heaviest
+// first instead).
+inline void plan_last_wave(Params& prm, int G) {
+  prm.tail_start = prm.num_units;
+  if (prm.num_splits == 1 && !prm.causal && ((prm.Nq + 127) / 128) % 2 == 0 &&
+      prm.num_units > G && prm.num_units <= INT_MAX - G) {
+    const int R = prm.num_units % G;
+    if (R > 0 && 2 * R <= G) {
+      prm.tail_start = prm.num_units - R;
+      prm.num_units += R;
+    }
+  }
 }
 
 // Shared-memory matrix descriptor (tcgen05 "matrix descriptor"): start
