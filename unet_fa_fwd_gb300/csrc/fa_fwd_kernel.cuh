@@ -355,8 +355,8 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
       ptx::tma_prefetch_desc(&p.tm_q);
       ptx::tma_prefetch_desc(&p.tm_k);
       ptx::tma_prefetch_desc(&p.tm_v);
-      uint32_t it = 0, uc = 0;
-      uint32_t issued[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+      uint32_t it = 0, uc = 0;        // K/V tiles handled so far, units started
+      uint32_t skipped = 0xffffffffu;  // the tile the stall hook withheld, if any
       uint32_t q_issued = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uc) {
@@ -379,7 +379,10 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
             ok = bounded_wait(ptx::smem_u32(&bars->kv_empty[s]), ph ^ 1, bars, p.timeout_ns);
             if (!ok) break;
             const uint32_t fb = ptx::smem_u32(&bars->kv_full[s]);
-            if (p.inject_stall && blockIdx.x == 0 && it == 3) continue;  // nothing arrives: consumers time out
+            if (p.inject_stall && blockIdx.x == 0 && it == 3) {  // nothing arrives: consumers time out
+              skipped = it;
+              continue;
+            }
             if (kv == 0) {
               ptx::mbar_arrive_expect_tx(fb, C::QK_TILE_BYTES);
               for (int c = 0; c < C::QK_NCHUNK; ++c)
@@ -391,19 +394,21 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
                 ptx::tma_load_3d(ptx::smem_u32(sRing + s * C::TILE_BYTES + c * C::CHUNK_BYTES),
                                  &p.tm_v, fb, c * C::CHUNK_ELEMS, (un.tile0 + j) * 128, bh);
             }
-            ++issued[s];
           }
         }
       }
       if (!ok) {
         // Drain: wait (bounded) until every copy this thread issued has landed.
+        // Stage s received the tiles k < it with k mod STAGES == s (less the
+        // withheld one); its barrier's last phase is that count minus one.
         const unsigned long long t_drain = p.timeout_ns;
         for (int s = 0; s < C::STAGES; ++s) {
-          if (issued[s] == 0) continue;
+          uint32_t n = it > (uint32_t)s ? (it - 1 - s) / C::STAGES + 1 : 0;
+          if (skipped < it && skipped % C::STAGES == (uint32_t)s) --n;
+          if (n == 0) continue;
           const uint32_t bar = ptx::smem_u32(&bars->kv_full[s]);
           uint64_t t0 = ptx::global_timer_ns();
-          while (!ptx::mbar_try_wait(bar, (issued[s] - 1) & 1) &&
-                 ptx::global_timer_ns() - t0 < t_drain) {
+          while (!ptx::mbar_try_wait(bar, (n - 1) & 1) && ptx::global_timer_ns() - t0 < t_drain) {
           }
         }
         if (q_issued) {
@@ -803,7 +808,12 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
         if (valid_row) row_lse += __ldg(p.lse_corr + (size_t)bh * p.Nq + qrow);
       }
       if (p.part_o == nullptr) {
-        __nv_bfloat16* orow = p.out + ((size_t)bh * p.Nq + (valid_row ? qrow : 0)) * D;
+        // Coalesced stores: thread = row in tensor memory, so each 32-column
+        // chunk (16 bf16 pairs per row) is transposed across the warp with
+        // shuffles; in pass q, lanes 4i..4i+3 write row 8q + i's 64 bytes as
+        // four consecutive 16-byte pieces (8 rows per store instruction).
+        const int warp_row0 = q0 + t * 128 + (warp % 4) * 32;  // query row of lane 0
+        const int piece = lane & 3;                             // 16-byte piece of the row
 #pragma unroll
         for (int cb = 0; cb < D; cb += 32) {
           uint32_t r[32];
@@ -813,12 +823,24 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
           for (int c = 0; c < 32; c += 2)
             packed[c / 2] = ptx::pack_bf16x2(__uint_as_float(r[c]) * inv_l,
                                              __uint_as_float(r[c + 1]) * inv_l);
-          if (valid_row) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + cb);
 #pragma unroll
-            for (int v4 = 0; v4 < 4; ++v4)
-              dst[v4] = make_uint4(packed[4 * v4], packed[4 * v4 + 1], packed[4 * v4 + 2],
-                                   packed[4 * v4 + 3]);
+          for (int q = 0; q < 4; ++q) {
+            const int src = 8 * q + (lane >> 2);  // lane (= row) whose piece this lane stores
+            uint32_t w[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              uint32_t v = 0;
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const uint32_t x = __shfl_sync(0xffffffffu, packed[4 * j + k], src);
+                if (piece == j) v = x;
+              }
+              w[k] = v;
+            }
+            const int orow = warp_row0 + src;
+            if (orow < p.Nq)
+              *reinterpret_cast<uint4*>(p.out + ((size_t)bh * p.Nq + orow) * D + cb + piece * 8) =
+                  make_uint4(w[0], w[1], w[2], w[3]);
           }
         }
         if (valid_row) p.lse[(size_t)bh * p.Nq + qrow] = row_lse;
