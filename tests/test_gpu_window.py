@@ -27,6 +27,9 @@ def _device():
     ((14, 21), (7, 7), (3, 3)),          # 7x7 windows, non-square grid
     ((32, 16), (16, 8), (5, 2)),         # 128-token windows
     ((12, 12), (12, 12), (0, 0)),        # one window = full attention
+    ((16, 16), (4, 4), (2, 2)),          # 16-token windows: 8 per 128-row batch entry
+    ((8, 8), (2, 2), (1, 1)),            # 4-token windows: 32 per entry
+    ((12, 8), (4, 4), (0, 0)),           # 12 windows in all: packing falls back to 6 per entry
 ])
 def test_window_parity(D, img, win, shift):
     base = {32: "page_example", 64: "sd_self", 128: "flux_1024"}[D]
