@@ -608,13 +608,6 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
         if (!ok) break;
         ++sc;
         ptx::tc_fence_after_sync();
-        float s[128];
-        {
-          uint32_t r[128];
-          ptx::tmem_ld32x32b_x128(tS, r);
-#pragma unroll
-          for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(r[c]);
-        }
         const int kbase = (un.tile0 + j) * 128;
         // log2-domain multiplier of raw S; with e4m3 Q and K it carries the
         // two block scales (positive, so its sign is the sign of `scale`).
@@ -622,14 +615,51 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
         if constexpr (F8)
           sl2 *= __ldg(p.q_scale + (size_t)bh * p.qtiles + (tile_row0 >> 7)) *
                  __ldg(p.k_scale + (size_t)bh * p.nkv + un.tile0 + j);
-        // Fast path: full key block, no mask, non-negative scale — the row max
-        // is taken on raw scores and scaled once.  Otherwise scores are
-        // materialised in the log2 domain with the mask and the Nk tail.
+        // Fast path: full key block, no mask, non-negative scale — the scores
+        // stay in registers and the row max is taken on raw scores, scaled
+        // once.  Otherwise (general path) scores are materialised in the log2
+        // domain with the mask, the Nk tail, the causal diagonal and segments.
         const bool general = (mask_b != nullptr) || any_full_mask || (kbase + 128 > p.Nk) ||
                              !(sl2 >= 0.f) || (p.causal && kbase + 127 > tile_row0) ||
                              p.seg > 0;
-        float mx;
+        auto release = [&](int h) {
+          ptx::tmem_wait_st();
+          ptx::tc_fence_before_sync();
+          ptx::mbar_arrive(h ? bar_p : bar_ph);
+        };
+        // Running-max update shared by both paths (sets alpha, m_use, rescale_o).
+        float alpha = 1.f, m_use = 0.f;
+        bool rescale_o = false;
+        auto update_max = [&](float mx) {
+          const float m_new = fmaxf(m, mx);
+          // Rescale only when the max grew by more than the threshold (or on the
+          // first finite max); otherwise keep the stale max, which is exact
+          // because the final O / l uses the same max.
+          const bool grow = (m_new - m) > kRescaleThreshold;  // -inf - -inf = NaN -> false
+          alpha = 1.f;
+          if (grow) {
+            alpha = ptx::ex2(m - m_new);  // m = -inf -> 0
+            m = m_new;
+          }
+          m_use = (m == -INFINITY) ? 0.f : m;
+          l *= alpha;
+          // P in two halves of 64 keys, each released as soon as it is in
+          // tensor memory so the first P·V MMAs overlap the second half's exp2.
+          // When O must be rescaled (rare: the max grew past the threshold) the
+          // first half waits until all of P is stored, so that the rescale runs
+          // with the scores already consumed.
+          rescale_o = j > 0 && __any_sync(0xffffffffu, grow);
+        };
+        float2 lsum = make_float2(0.f, 0.f);
         if (!general) {
+          float s[128];  // the fast path keeps the scores in registers
+          float mx;
+          {
+            uint32_t r[128];
+            ptx::tmem_ld32x32b_x128(tS, r);
+#pragma unroll
+            for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(r[c]);
+          }
           float a0 = s[0], a1 = s[1], a2 = s[2], a3 = s[3];
 #pragma unroll
           for (int c = 4; c < 128; c += 8) {
@@ -639,107 +669,7 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
             a3 = ptx::fmax3(a3, s[c + 6], s[c + 7]);
           }
           mx = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)) * sl2;
-        } else {
-          mx = -INFINITY;
-          // This row of the per-(query, key) mask (rows past Nq read nothing).
-          const float* fmask_f = nullptr;
-          const uint8_t* fmask_b = nullptr;
-          if (any_full_mask && qrow < p.Nq) {
-            const size_t fm_row =
-                ((size_t)(bh / p.H) * p.mask_heads + (p.mask_heads == 1 ? 0 : bh % p.H)) * p.Nq +
-                (size_t)qrow;
-            if (p.full_mask_bool)
-              fmask_b = static_cast<const uint8_t*>(p.full_mask) + fm_row * p.Nk;
-            else
-              fmask_f = static_cast<const float*>(p.full_mask) + fm_row * p.Nk;
-          }
-          // Masks are read 8 keys at a time: two 16-byte loads of fp32, one
-          // 8-byte load of uint8, when the 8 keys lie inside Nk and every row
-          // start is aligned (base pointer aligned and Nk a multiple of 4 / 8;
-          // the C ABI admits 4-byte-aligned fp32 and unaligned uint8 masks);
-          // scalar loads otherwise.
-          // Keys of this row's segment (all keys when rows are not segmented).
-          const int seg_lo = p.seg > 0 ? (qrow / p.seg) * p.seg : 0;
-          const int seg_hi = p.seg > 0 ? seg_lo + p.seg : p.Nk;
-          const float* madd_base = p.mask ? p.mask : (p.full_mask_bool ? nullptr
-                                                      : static_cast<const float*>(p.full_mask));
-          const bool vec_f = (p.Nk & 3) == 0 && (reinterpret_cast<uintptr_t>(madd_base) & 15u) == 0;
-          const bool vec_b = (p.Nk & 7) == 0 && (reinterpret_cast<uintptr_t>(p.full_mask) & 7u) == 0;
-#pragma unroll
-          for (int cb = 0; cb < 128; cb += 8) {
-            const int key0 = kbase + cb;
-            const bool whole = key0 + 8 <= p.Nk;
-            float add[8];
-            bool keep[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              add[i] = 0.f;
-              keep[i] = true;
-            }
-            const float* madd = mask_b ? mask_b : fmask_f;  // at most one additive mask
-            if (madd) {
-              if (whole && vec_f) {
-                const float4 a = __ldg(reinterpret_cast<const float4*>(madd + key0));
-                const float4 b = __ldg(reinterpret_cast<const float4*>(madd + key0 + 4));
-                add[0] = a.x; add[1] = a.y; add[2] = a.z; add[3] = a.w;
-                add[4] = b.x; add[5] = b.y; add[6] = b.z; add[7] = b.w;
-              } else {
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                  if (key0 + i < p.Nk) add[i] = __ldg(madd + key0 + i);
-              }
-            }
-            if (fmask_b) {
-              if (whole && vec_b) {
-                const uint2 v = __ldg(reinterpret_cast<const uint2*>(fmask_b + key0));
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                  keep[i] = ((v.x >> (8 * i)) & 0xffu) != 0u;
-                  keep[4 + i] = ((v.y >> (8 * i)) & 0xffu) != 0u;
-                }
-              } else {
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                  if (key0 + i < p.Nk) keep[i] = __ldg(fmask_b + key0 + i) != 0;
-              }
-            }
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const int key = key0 + i;
-              float tv = -INFINITY;
-              if (key < p.Nk && !(p.causal && key > qrow) && keep[i] && key >= seg_lo &&
-                  key < seg_hi)
-                tv = fmaf(add[i], kLog2e, s[cb + i] * sl2);
-              s[cb + i] = tv;
-              mx = fmaxf(mx, tv);
-            }
-          }
-        }
-        const float m_new = fmaxf(m, mx);
-        // Rescale only when the max grew by more than the threshold (or on the
-        // first finite max); otherwise keep the stale max, which is exact
-        // because the final O / l uses the same max.
-        const bool grow = (m_new - m) > kRescaleThreshold;  // -inf - -inf = NaN -> false
-        float alpha = 1.f;
-        if (grow) {
-          alpha = ptx::ex2(m - m_new);  // m = -inf -> 0
-          m = m_new;
-        }
-        const float m_use = (m == -INFINITY) ? 0.f : m;
-        l *= alpha;
-        // P in two halves of 64 keys, each released as soon as it is in
-        // tensor memory so the first P·V MMAs overlap the second half's exp2.
-        // When O must be rescaled (rare: the max grew past the threshold) the
-        // first half waits until all of P is stored, so that the rescale runs
-        // with the scores already consumed.
-        const bool rescale_o = j > 0 && __any_sync(0xffffffffu, grow);
-        auto release = [&](int h) {
-          ptx::tmem_wait_st();
-          ptx::tc_fence_before_sync();
-          ptx::mbar_arrive(h ? bar_p : bar_ph);
-        };
-        float2 lsum = make_float2(0.f, 0.f);
-        if (!general) {
+          update_max(mx);
           const float2 sc2 = make_float2(sl2, sl2);
           const float2 nm2 = make_float2(-m_use, -m_use);
 #pragma unroll
@@ -762,13 +692,106 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
             if (cb == 32 && !rescale_o) release(0);
           }
         } else {
+          float mx;
+          // General path, compact: two rolled loops over the S block in tensor
+          // memory (this path runs on masked, causal-diagonal, Nk-tail and
+          // packed-window blocks, often enough that unrolled code would not stay
+          // in the instruction cache).  Pass 1 turns 16 scores at a time into
+          // log2-domain values with excluded pairs at -inf, keeps their max and
+          // writes them back; pass 2 (below) takes their exponentials.
+          mx = -INFINITY;
+          // This row of the per-(query, key) mask (rows past Nq read nothing).
+          const float* fmask_f = nullptr;
+          const uint8_t* fmask_b = nullptr;
+          if (any_full_mask && qrow < p.Nq) {
+            const size_t fm_row =
+                ((size_t)(bh / p.H) * p.mask_heads + (p.mask_heads == 1 ? 0 : bh % p.H)) * p.Nq +
+                (size_t)qrow;
+            if (p.full_mask_bool)
+              fmask_b = static_cast<const uint8_t*>(p.full_mask) + fm_row * p.Nk;
+            else
+              fmask_f = static_cast<const float*>(p.full_mask) + fm_row * p.Nk;
+          }
+          // Keys of this row's segment (all keys when rows are not segmented).
+          const int seg_lo = p.seg > 0 ? (qrow / p.seg) * p.seg : 0;
+          const int seg_hi = p.seg > 0 ? seg_lo + p.seg : p.Nk;
+          // Masks are read 8 keys per load: two 16-byte loads of fp32, one
+          // 8-byte load of uint8, when the 8 keys lie inside Nk and every row
+          // start is aligned (base pointer aligned and Nk a multiple of 4 / 8;
+          // the C ABI admits 4-byte-aligned fp32 and unaligned uint8 masks);
+          // scalar loads otherwise.
+          const float* madd = mask_b ? mask_b : fmask_f;  // at most one additive mask
+          const float* madd_base = p.mask ? p.mask : (p.full_mask_bool ? nullptr
+                                                      : static_cast<const float*>(p.full_mask));
+          const bool vec_f = (p.Nk & 3) == 0 && (reinterpret_cast<uintptr_t>(madd_base) & 15u) == 0;
+          const bool vec_b = (p.Nk & 7) == 0 && (reinterpret_cast<uintptr_t>(p.full_mask) & 7u) == 0;
+#pragma unroll 1
+          for (int cb = 0; cb < 128; cb += 16) {
+            uint32_t r[16];
+            ptx::tmem_ld32x32b_x16(tS + cb, r);
+            float add[16];
+            uint32_t keepbits = 0xffffu;  // bit i: key cb + i kept by the bool mask
 #pragma unroll
+            for (int i = 0; i < 16; ++i) add[i] = 0.f;
+#pragma unroll
+            for (int h = 0; h < 16; h += 8) {
+              const int key0 = kbase + cb + h;
+              const bool whole = key0 + 8 <= p.Nk;
+              if (madd) {
+                if (whole && vec_f) {
+                  const float4 a = __ldg(reinterpret_cast<const float4*>(madd + key0));
+                  const float4 b = __ldg(reinterpret_cast<const float4*>(madd + key0 + 4));
+                  add[h + 0] = a.x; add[h + 1] = a.y; add[h + 2] = a.z; add[h + 3] = a.w;
+                  add[h + 4] = b.x; add[h + 5] = b.y; add[h + 6] = b.z; add[h + 7] = b.w;
+                } else {
+#pragma unroll
+                  for (int i = 0; i < 8; ++i)
+                    if (key0 + i < p.Nk) add[h + i] = __ldg(madd + key0 + i);
+                }
+              }
+              if (fmask_b) {
+                if (whole && vec_b) {
+                  const uint2 v = __ldg(reinterpret_cast<const uint2*>(fmask_b + key0));
+#pragma unroll
+                  for (int i = 0; i < 4; ++i) {
+                    if (((v.x >> (8 * i)) & 0xffu) == 0u) keepbits &= ~(1u << (h + i));
+                    if (((v.y >> (8 * i)) & 0xffu) == 0u) keepbits &= ~(1u << (h + 4 + i));
+                  }
+                } else {
+#pragma unroll
+                  for (int i = 0; i < 8; ++i)
+                    if (key0 + i < p.Nk && __ldg(fmask_b + key0 + i) == 0)
+                      keepbits &= ~(1u << (h + i));
+                }
+              }
+            }
+            uint32_t tv_bits[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int key = kbase + cb + i;
+              float tv = -INFINITY;
+              if (key < p.Nk && !(p.causal && key > qrow) && ((keepbits >> i) & 1u) &&
+                  key >= seg_lo && key < seg_hi)
+                tv = fmaf(add[i], kLog2e, __uint_as_float(r[i]) * sl2);
+              mx = fmaxf(mx, tv);
+              tv_bits[i] = __float_as_uint(tv);
+            }
+            ptx::tmem_st32x32b_x16(tS + cb, tv_bits);
+          }
+          ptx::tmem_wait_st();  // pass 2 reads these columns back
+          update_max(mx);
+          // Pass 2 of the general path: exponentials of the log2-domain values
+          // pass 1 left in tensor memory; P (bf16 pairs) goes over the first 64
+          // columns, behind the columns still to be read.
+#pragma unroll 1
           for (int cb = 0; cb < 128; cb += 32) {
+            uint32_t r[32];
+            ptx::tmem_ld32x32b_x32(tS + cb, r);
             uint32_t packed[16];
 #pragma unroll
             for (int c = 0; c < 32; c += 2) {
-              const float p0 = ptx::ex2(s[cb + c] - m_use);
-              const float p1 = ptx::ex2(s[cb + c + 1] - m_use);
+              const float p0 = ptx::ex2(__uint_as_float(r[c]) - m_use);
+              const float p1 = ptx::ex2(__uint_as_float(r[c + 1]) - m_use);
               lsum = __fadd2_rn(lsum, make_float2(p0, p1));
               packed[c / 2] = ptx::pack_bf16x2(p0, p1);
             }
