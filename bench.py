@@ -371,8 +371,18 @@ def bench_native(args, world, rank, local):
                            "ms_max": round(max(times), 4), "tflops": round(sfl / med / 1e9, 1),
                            "hbm_gbs": round(sby / med / 1e6, 1),
                            "hbm_frac": round(sby / med / 1e6 / hbm, 4)}
+            if name in ("page_example", "sd_cross"):
+                # launch-bound sizes: also 1000 launches back to back (inputs L2-resident)
+                b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                b0.record(stream)
+                for _ in range(1000):
+                    call()
+                b1.record(stream)
+                torch.cuda.synchronize(device)
+                small[name]["us_per_launch_back_to_back"] = round(b0.elapsed_time(b1), 3)
             del w_in, so_, sl_
-        also["small_configs"] = {"l2": "flushed (256 MB write) before every timed launch",
+        also["small_configs"] = {"l2": "flushed (256 MB write) before every timed launch; "
+                                       "us_per_launch_back_to_back: 1000 launches, L2-resident",
                                  "launches": 30, "configs": small}
         del flush
 
