@@ -46,7 +46,8 @@ def _load():
         lib.fa_oracle_window.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, dp, dp, i32,
                                          i32, i32, f64, i32]
         lib.fa_oracle_window.restype = i32
-        lib.fa_oracle_probs.argtypes = [vp, vp, vp, i32, i32, i32, i32, dp, i32, i32, i32, i32, i32, f64]
+        lib.fa_oracle_probs.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, dp, dp, dp, i32, i32,
+                                        i32, i32, i32, f64]
         lib.fa_oracle_probs.restype = i32
         _lib = lib
     return _lib
@@ -196,23 +197,28 @@ def window_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, img_h: int, im
     return out, lse
 
 
-def probs(q: np.ndarray, k: np.ndarray, b: int, h: int, i: int, mask: np.ndarray | None = None,
-          scale: float | None = None) -> np.ndarray:
-    """Softmax row p_ij (fp64, length Nk) of query (b, h, i)."""
+def probs(q: np.ndarray, k: np.ndarray, v: np.ndarray, b: int, h: int, i: int,
+          mask: np.ndarray | None = None, scale: float | None = None):
+    """Row (b, h, i) through the oracle's own row function: returns (p, o_row, lse) with
+    p the softmax row p_ij (fp64, length Nk), o_row the O row (fp64, length D)."""
     lib = _load()
     B, H, Nq, D = q.shape
     Nk = k.shape[2]
     qa, dt = _as_input(q)
     ka, dtk = _as_input(k)
-    if dt != dtk:
-        raise TypeError("q, k must share one dtype")
+    va, dtv = _as_input(v)
+    if not (dt == dtk == dtv):
+        raise TypeError("q, k, v must share one dtype")
     m = None if mask is None else np.ascontiguousarray(mask, dtype=np.float32)
     if scale is None:
         scale = 1.0 / np.sqrt(D)
+    dp = ctypes.POINTER(ctypes.c_double)
     p = np.empty(Nk, dtype=np.float64)
-    rc = lib.fa_oracle_probs(_ptr(qa), _ptr(ka), _ptr(m), dt, b, h, i,
-                             p.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
+    o_row = np.empty(D, dtype=np.float64)
+    lse = ctypes.c_double(0.0)
+    rc = lib.fa_oracle_probs(_ptr(qa), _ptr(ka), _ptr(va), _ptr(m), dt, b, h, i,
+                             p.ctypes.data_as(dp), o_row.ctypes.data_as(dp), ctypes.byref(lse),
                              B, H, Nq, Nk, D, float(scale))
     if rc != 0:
         raise RuntimeError(f"oracle probs failed with code {rc}")
-    return p
+    return p, o_row, lse.value

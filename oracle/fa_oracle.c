@@ -99,9 +99,11 @@ static int64_t window_of(const oracle_job* job, int64_t t) {
 }
 
 /* One query row of one head: materialise the score row, then softmax, then the
- * weighted sum of V rows.  s and p are scratch buffers of length Nk. */
+ * weighted sum of V rows.  s and p are scratch buffers of length Nk.  When
+ * probs_out is not NULL the row's softmax probabilities p_j / l are also
+ * written there (all zeros for a fully masked row). */
 static void attend_one_row(const oracle_job* job, int64_t bh, int64_t i, double* o_row,
-                           double* lse_out, double* s, double* p) {
+                           double* lse_out, double* s, double* p, double* probs_out) {
     const int Nk = job->Nk, D = job->D, Nq = job->Nq;
     const int64_t b = bh / job->H;
     const int64_t q_base = (bh * Nq + i) * D;
@@ -133,6 +135,8 @@ static void attend_one_row(const oracle_job* job, int64_t bh, int64_t i, double*
     if (m == -INFINITY) { /* every key masked */
         for (int d = 0; d < D; ++d) o_row[d] = 0.0;
         *lse_out = -INFINITY;
+        if (probs_out)
+            for (int j = 0; j < Nk; ++j) probs_out[j] = 0.0;
         return;
     }
 
@@ -152,6 +156,8 @@ static void attend_one_row(const oracle_job* job, int64_t bh, int64_t i, double*
     for (int d = 0; d < D; ++d) o_row[d] /= l;
 
     *lse_out = m + log(l);
+    if (probs_out)
+        for (int j = 0; j < Nk; ++j) probs_out[j] = p[j] / l;
 }
 
 static void* worker(void* arg) {
@@ -170,7 +176,7 @@ static void* worker(void* arg) {
         int64_t bh = item / per_head;
         int64_t r = item % per_head;
         int64_t i = job->rows ? job->rows[bh * job->nrows + r] : r;
-        attend_one_row(job, bh, i, job->out + item * job->D, job->lse + item, s, p);
+        attend_one_row(job, bh, i, job->out + item * job->D, job->lse + item, s, p, NULL);
     }
     free(s);
     free(p);
@@ -275,35 +281,29 @@ int fa_oracle_window(const void* q, const void* k, const void* v, int dtype, int
     return run_job(&job, nthreads);
 }
 
-/* The softmax probabilities of one row (b, h, i): p_j = exp(s_ij - m_i) / l_i,
- * written to probs[Nk].  A fully masked row gives all zeros.  Used to check
- * that each row of the attention matrix is a probability distribution. */
-int fa_oracle_probs(const void* q, const void* k, const float* mask, int dtype, int b, int h,
-                    int i, double* probs, int B, int H, int Nq, int Nk, int D, double scale) {
-    if (!q || !k || !probs || check_shape(B, H, Nq, Nk, D)) return 1;
+/* One row (b, h, i) of the forward through the same function every other
+ * entry point uses (attend_one_row), also returning that row's softmax
+ * probabilities p_j = exp(s_ij - m_i) / l_i in probs[Nk] (all zeros for a
+ * fully masked row), its O row in o_row[D] and its LSE.  Used to check that
+ * each row of the attention matrix is a probability distribution and that
+ * O_i = sum_j p_j v_j. */
+int fa_oracle_probs(const void* q, const void* k, const void* v, const float* mask, int dtype,
+                    int b, int h, int i, double* probs, double* o_row, double* lse, int B, int H,
+                    int Nq, int Nk, int D, double scale) {
+    if (!q || !k || !v || !probs || !o_row || !lse || check_shape(B, H, Nq, Nk, D)) return 1;
+    if (dtype != ORACLE_DTYPE_F32 && dtype != ORACLE_DTYPE_BF16) return 1;
     if (b < 0 || b >= B || h < 0 || h >= H || i < 0 || i >= Nq) return 1;
-    const int64_t bh = (int64_t)b * H + h;
-    const int64_t q_base = (bh * Nq + i) * D;
-    const int64_t k_base = bh * (int64_t)Nk * D;
-    double m = -INFINITY;
-    for (int j = 0; j < Nk; ++j) {
-        double dot = 0.0;
-        for (int d = 0; d < D; ++d)
-            dot += load_elem(q, dtype, q_base + d) * load_elem(k, dtype, k_base + (int64_t)j * D + d);
-        double sij = scale * dot;
-        if (mask) sij += (double)mask[(int64_t)b * Nk + j];
-        probs[j] = sij;
-        if (sij > m) m = sij;
+    oracle_job job = {q, k, v, mask, NULL, 1, 0, 0, 0, 0, 0, 0, 0, 0, dtype, B, H, Nq, Nk, D, scale,
+                      NULL, 0, NULL, NULL, 1, 0};
+    double* s = (double*)malloc(sizeof(double) * (size_t)Nk);
+    double* p = (double*)malloc(sizeof(double) * (size_t)Nk);
+    if (!s || !p) {
+        free(s);
+        free(p);
+        return 2;
     }
-    if (m == -INFINITY) {
-        for (int j = 0; j < Nk; ++j) probs[j] = 0.0;
-        return 0;
-    }
-    double l = 0.0;
-    for (int j = 0; j < Nk; ++j) {
-        probs[j] = exp(probs[j] - m);
-        l += probs[j];
-    }
-    for (int j = 0; j < Nk; ++j) probs[j] /= l;
+    attend_one_row(&job, (int64_t)b * H + h, i, o_row, lse, s, p, probs);
+    free(s);
+    free(p);
     return 0;
 }

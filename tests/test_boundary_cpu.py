@@ -165,3 +165,58 @@ def test_fp8_validation_before_any_cuda_call(lib):
 
 def test_ex2_probe_validation_before_any_cuda_call(lib):
     assert lib.fa_measure_ex2_rate(None, None) == 1   # FA_ERR_INVALID_ARGUMENT
+
+
+def _noalloc_call(**kw):
+    a = dict(FAKE, num_splits=4)
+    a.update(kw)
+    fn = fa.load_library().fa_fwd_split_noalloc
+    vp, i32 = ctypes.c_void_p, ctypes.c_int
+    fn.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, ctypes.c_float, i32, vp]
+    fn.restype = i32
+    return fn(a["q"], a["k"], a["v"], a["mask"], a["out"], a["lse"], a["B"], a["H"], a["Nq"],
+              a["Nk"], a["D"], a["scale"], a["num_splits"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(num_splits=0), 1), (dict(num_splits=-3), 1), (dict(Nk=0), 1), (dict(B=0), 1),
+    (dict(Nq=0), 1), (dict(q=None), 1), (dict(q=None, Nk=1000), 1), (dict(lse=None), 1),
+    (dict(out=0x10000), 1), (dict(scale=float("nan")), 1), (dict(D=48), 2),
+    (dict(D=48, Nk=1000), 2),
+    # 8 heads x 4096 queries x 8 ranges of fp32 partials do not fit the 32 MiB scratch
+    (dict(B=1, H=8, Nq=4096, Nk=2048, D=128, num_splits=8, q=1 << 40, k=2 << 40, v=3 << 40,
+          out=4 << 40, lse=5 << 40), 1),
+])
+def test_noalloc_validation_before_any_cuda_call(lib, kw, code):
+    """Every rejection of fa_fwd_split_noalloc happens before its first CUDA call
+    (on this machine without a driver a CUDA call would answer FA_ERR_CUDA)."""
+    assert _noalloc_call(**kw) == code
+
+
+def test_noalloc_valid_call_without_gpu_reports_cuda_error(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert _noalloc_call(Nk=100, num_splits=1) == 3     # one range: the plain forward's set-up
+    far = dict(q=1 << 40, k=2 << 40, v=3 << 40, out=4 << 40, lse=5 << 40)
+    assert _noalloc_call(Nk=1000, num_splits=4, **far) == 3    # scratch look-up
+
+
+def test_split_unit_count_overflow_rejected_before_any_cuda_call(lib):
+    # B*H = 2^24 heads x 1 query pair x 256 key ranges = 2^32 work units > INT_MAX.
+    ptrs = dict(q=1 << 47, k=2 << 47, v=3 << 47, out=4 << 47, lse=5 << 47)
+    raw = fa.load_library()
+    rc = raw.fa_fwd_split(ptrs["q"], ptrs["k"], ptrs["v"], None, ptrs["out"], ptrs["lse"],
+                          1 << 14, 1 << 10, 256, 256 * 128, 64, ctypes.c_float(0.125), 256,
+                          1 << 52, 1 << 60, None)
+    assert rc == 1
+
+
+def test_window_fault_hook_enqueues_nothing(lib, monkeypatch):
+    """With valid arguments the window path sets up (where the launch hook fires)
+    before its first kernel is enqueued."""
+    monkeypatch.setenv("FA_FAULT_INJECT", "launch")
+    raw = fa.load_library()
+    rc = raw.fa_fwd_window(0x10000, 0x20000, 0x30000, 0x40000, 0x50000, 1, 2, 8, 8, 64, 4, 4, 0, 0,
+                           ctypes.c_float(0.1), 0xA0000, 1 << 20, None)
+    assert rc == 3

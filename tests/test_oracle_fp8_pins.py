@@ -97,3 +97,78 @@ def test_fully_masked_row_in_emulation():
     o8, l8 = fp8.attention_fp8_emulated(q, k, v, mask=mask)
     assert np.all(o8[1] == 0) and np.all(np.isneginf(l8[1]))
     assert np.all(np.isfinite(l8[0]))
+
+
+def _scaled_grid_blocks(rng, BH, N, D, exps, max_rows, negate_pairs=False):
+    """[BH, N, D] with every 128-row block b on the e4m3 grid times 2^-exps[b] and its
+    largest magnitude exactly 448 * 2^-exps[b], placed at row max_rows[b] of the block.
+    With negate_pairs, the second 64 rows of each full block are the negatives of the
+    first 64, so every block (and the whole tensor) has channel sums exactly 0."""
+    vals = np.array([x for x, _ in _e4m3_values()])
+    small = vals[vals <= 8.0]
+    x = np.empty((BH, N, D))
+    for b, e in enumerate(exps):
+        r0, r1 = 128 * b, min(128 * (b + 1), N)
+        n = r1 - r0
+        half = n // 2 if negate_pairs else n
+        blk = rng.choice(small, size=(BH, half, D)) * rng.choice([-1.0, 1.0], size=(BH, half, D))
+        blk[:, max_rows[b] % half, b % D] = 448.0
+        if negate_pairs:
+            assert n % 2 == 0
+            blk = np.concatenate([blk, -blk], axis=1)
+        x[:, r0:r1] = blk * 2.0 ** -e
+    return x
+
+
+def test_block_scales_are_per_block_and_per_operand():
+    """Q blocks with maxima 448·2^0, 448·2^-2, 448·2^-5 (the last block ragged) and K
+    blocks with 448·2^-1, 448·2^-3: every block scale is a distinct power of two, so
+    each block's scaled values land back on the e4m3 grid and quantisation is exact —
+    but only if each 128-row block gets its own scale.  A wrong block size (the maxima
+    sit in different 64-row halves), a wrong block index, or the Q and K scales
+    swapped would round values off the grid or mis-scale scores, and the emulation
+    would no longer equal the exact attention."""
+    rng = np.random.default_rng(11)
+    B, H, Nq, Nk, D = 1, 2, 300, 256, 32
+    q = _scaled_grid_blocks(rng, B * H, Nq, D, exps=[0, 2, 5], max_rows=[3, 100, 40])
+    k = _scaled_grid_blocks(rng, B * H, Nk, D, exps=[1, 3], max_rows=[70, 5], negate_pairs=True)
+    q = q.reshape(B, H, Nq, D).astype(np.float32)
+    k = k.reshape(B, H, Nk, D).astype(np.float32)
+    v = rng.standard_normal((B, H, Nk, D)).astype(np.float32)
+    assert np.all(k.astype(np.float64).sum(axis=2) == 0)        # smoothing is a no-op
+    # the per-block scales the emulation derives are the planted powers of two
+    _, sq = fp8._quantise_blocks(q.reshape(B * H, Nq, D))
+    _, sk = fp8._quantise_blocks(k.reshape(B * H, Nk, D))
+    np.testing.assert_array_equal(sq, np.tile([1.0, 2.0 ** -2, 2.0 ** -5], (B * H, 1)))
+    np.testing.assert_array_equal(sk, np.tile([2.0 ** -1, 2.0 ** -3], (B * H, 1)))
+    scale = 2.0 ** -12
+    o8, l8 = fp8.attention_fp8_emulated(q, k, v, scale=scale)
+    o, l = oracle.attention(q, k, v, scale=scale)
+    np.testing.assert_allclose(o8, o, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l8, l, rtol=1e-12, atol=1e-12)
+
+
+def test_mean_smoothing_lse_correction_is_exact():
+    """K = K0 + c with K0 on the e4m3 grid (zero channel sums) and c an exactly
+    representable per-channel offset: the emulation recovers c exactly as the mean,
+    quantises K0 without error, and must add scale · q_i · c back to LSE — giving the
+    exact attention's O and LSE to rounding (the offset moves every score of row i
+    by the same scale · q_i · c, which the softmax ignores and LSE carries)."""
+    rng = np.random.default_rng(12)
+    B, H, Nq, Nk, D = 1, 2, 200, 256, 32
+    q = _scaled_grid_blocks(rng, B * H, Nq, D, exps=[0, 1], max_rows=[9, 60])
+    k0 = _scaled_grid_blocks(rng, B * H, Nk, D, exps=[2, 0], max_rows=[1, 33], negate_pairs=True)
+    c = rng.integers(-12, 13, size=(B * H, 1, D)) * 0.25          # multiples of 1/4 in [-3, 3]
+    c[:, 0, 0] = 2.75                                             # never all zero
+    q = q.reshape(B, H, Nq, D).astype(np.float32)
+    k = (k0 + c).reshape(B, H, Nk, D).astype(np.float32)
+    assert np.array_equal(k.astype(np.float64), (k0 + c).reshape(B, H, Nk, D))   # exact in fp32
+    v = rng.standard_normal((B, H, Nk, D)).astype(np.float32)
+    scale = 2.0 ** -11
+    o8, l8 = fp8.attention_fp8_emulated(q, k, v, scale=scale)
+    o, l = oracle.attention(q, k, v, scale=scale)
+    np.testing.assert_allclose(o8, o, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l8, l, rtol=1e-12, atol=1e-11)
+    # the correction is really exercised: it moves LSE by far more than the tolerance
+    shift = scale * np.einsum("hnd,hd->hn", q.reshape(B * H, Nq, D).astype(np.float64), c[:, 0])
+    assert np.abs(shift).max() > 1e-2

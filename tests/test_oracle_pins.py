@@ -148,16 +148,25 @@ def test_blocked_equals_definition(Nq, Nk, D, bq, bk, masked):
 # ---------------------------------------------------------------------------
 
 def test_probability_rows_sum_to_one():
+    """The p_j of the oracle's row function (the one every forward entry point
+    runs) form a probability distribution, are 0 on masked keys, and weight the
+    V rows into exactly the O row the forward returns."""
     rng = _rng(1)
-    q, k = _randn(rng, 1, 2, 7, 16), _randn(rng, 1, 2, 33, 16)
+    q, k, v = _randn(rng, 1, 2, 7, 16), _randn(rng, 1, 2, 33, 16), _randn(rng, 1, 2, 33, 16)
     mask = np.zeros((1, 33), np.float32)
     mask[0, 20:] = -np.inf
+    o_all, lse_all = oracle.attention(q, k, v, mask=mask)
     for h in range(2):
         for i in range(7):
-            p = oracle.probs(q, k, 0, h, i, mask=mask)
+            p, o_row, lse = oracle.probs(q, k, v, 0, h, i, mask=mask)
             assert abs(p.sum() - 1.0) < 1e-12
             assert np.all(p >= 0)
             assert np.all(p[20:] == 0)
+            assert np.array_equal(o_row, o_all[0, h, i]) and lse == lse_all[0, h, i]
+            assert np.max(np.abs(p @ v[0, h].astype(np.float64) - o_row)) < 1e-12
+    mask[0, :] = -np.inf
+    p, o_row, lse = oracle.probs(q, k, v, 0, 1, 3, mask=mask)
+    assert np.all(p == 0) and np.all(o_row == 0) and lse == -np.inf
 
 
 @pytest.mark.parametrize("how", ["zero_q", "zero_scale"])

@@ -142,11 +142,16 @@ int launch_merge(const float* part_o, const float* part_lse, __nv_bfloat16* out,
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
-// Validation and set-up shared by the entry points.  On success `prm` holds
-// the tensor maps and sizes of an unsplit launch and `st` the device state.
-int prepare(const void* q, const void* k, const void* v, const float* mask, void* out, float* lse,
-            int B, int H, int Nq, int Nk, int D, float scale, fa::Params* prm, DeviceState** st) {
-  // ---- validation: no CUDA call before this block passes ----
+// Sizes of one validated problem (no CUDA call was needed to get them).
+struct Shape {
+  int64_t BH, upb;
+  size_t q_bytes, kv_bytes, lse_bytes, mask_bytes;
+};
+
+// Validation shared by the entry points; makes no CUDA call, so an invalid
+// call returns before anything touches the device.
+int validate(const void* q, const void* k, const void* v, const float* mask, const void* out,
+             const float* lse, int B, int H, int Nq, int Nk, int D, float scale, Shape* sh) {
   if (!q || !k || !v || !out || !lse) return FA_ERR_INVALID_ARGUMENT;
   if (B < 1 || H < 1 || Nq < 1 || Nk < 1) return FA_ERR_INVALID_ARGUMENT;
   if (!std::isfinite(scale)) return FA_ERR_INVALID_ARGUMENT;
@@ -158,17 +163,37 @@ int prepare(const void* q, const void* k, const void* v, const float* mask, void
   const int64_t qtiles = ((int64_t)Nq + 127) / 128;
   const int64_t upb = (qtiles + 1) / 2;
   if (BH > INT_MAX || BH * upb > INT_MAX || BH > (int64_t)UINT32_MAX) return FA_ERR_INVALID_ARGUMENT;
-  const size_t q_bytes = (size_t)BH * Nq * D * 2, kv_bytes = (size_t)BH * Nk * D * 2;
-  const size_t lse_bytes = (size_t)BH * Nq * 4, mask_bytes = mask ? (size_t)B * Nk * 4 : 0;
-  if (ranges_overlap(out, q_bytes, q, q_bytes) || ranges_overlap(out, q_bytes, k, kv_bytes) ||
-      ranges_overlap(out, q_bytes, v, kv_bytes) || ranges_overlap(out, q_bytes, lse, lse_bytes) ||
-      ranges_overlap(out, q_bytes, mask, mask_bytes) ||
-      ranges_overlap(lse, lse_bytes, q, q_bytes) || ranges_overlap(lse, lse_bytes, k, kv_bytes) ||
-      ranges_overlap(lse, lse_bytes, v, kv_bytes) ||
-      ranges_overlap(lse, lse_bytes, mask, mask_bytes))
+  sh->BH = BH;
+  sh->upb = upb;
+  sh->q_bytes = (size_t)BH * Nq * D * 2;
+  sh->kv_bytes = (size_t)BH * Nk * D * 2;
+  sh->lse_bytes = (size_t)BH * Nq * 4;
+  sh->mask_bytes = mask ? (size_t)B * Nk * 4 : 0;
+  const size_t qb = sh->q_bytes, kvb = sh->kv_bytes, lb = sh->lse_bytes, mb = sh->mask_bytes;
+  if (ranges_overlap(out, qb, q, qb) || ranges_overlap(out, qb, k, kvb) ||
+      ranges_overlap(out, qb, v, kvb) || ranges_overlap(out, qb, lse, lb) ||
+      ranges_overlap(out, qb, mask, mb) || ranges_overlap(lse, lb, q, qb) ||
+      ranges_overlap(lse, lb, k, kvb) || ranges_overlap(lse, lb, v, kvb) ||
+      ranges_overlap(lse, lb, mask, mb))
     return FA_ERR_INVALID_ARGUMENT;
+  return FA_OK;
+}
 
-  // ---- set-up ----
+// A workspace must not overlap any buffer of the call.
+bool workspace_overlaps(const void* ws, size_t ws_bytes, const void* q, const void* k,
+                        const void* v, const float* mask, const void* out, const float* lse,
+                        const Shape& sh) {
+  return ranges_overlap(ws, ws_bytes, q, sh.q_bytes) || ranges_overlap(ws, ws_bytes, k, sh.kv_bytes) ||
+         ranges_overlap(ws, ws_bytes, v, sh.kv_bytes) || ranges_overlap(ws, ws_bytes, out, sh.q_bytes) ||
+         ranges_overlap(ws, ws_bytes, lse, sh.lse_bytes) ||
+         ranges_overlap(ws, ws_bytes, mask, sh.mask_bytes);
+}
+
+// Set-up of a validated call (CUDA calls, nothing enqueued): device state and
+// the tensor maps and sizes of an unsplit launch.
+int setup(const void* q, const void* k, const void* v, const float* mask, void* out, float* lse,
+          int H, int Nq, int Nk, int D, float scale, const Shape& sh, fa::Params* prm,
+          DeviceState** st) {
   const char* inject = std::getenv("FA_FAULT_INJECT");
   if (inject && std::strcmp(inject, "launch") == 0) return FA_ERR_CUDA;
   int dev = 0;
@@ -178,9 +203,9 @@ int prepare(const void* q, const void* k, const void* v, const float* mask, void
   if (!(*st)->supported) return FA_ERR_UNSUPPORTED;
 
   std::memset(prm, 0, sizeof(*prm));
-  if (encode_map(&prm->tm_q, q, (int)BH, Nq, D) != FA_OK ||
-      encode_map(&prm->tm_k, k, (int)BH, Nk, D) != FA_OK ||
-      encode_map(&prm->tm_v, v, (int)BH, Nk, D) != FA_OK)
+  if (encode_map(&prm->tm_q, q, (int)sh.BH, Nq, D) != FA_OK ||
+      encode_map(&prm->tm_k, k, (int)sh.BH, Nk, D) != FA_OK ||
+      encode_map(&prm->tm_v, v, (int)sh.BH, Nk, D) != FA_OK)
     return FA_ERR_CUDA;
   prm->out = reinterpret_cast<__nv_bfloat16*>(out);
   prm->lse = lse;
@@ -188,12 +213,12 @@ int prepare(const void* q, const void* k, const void* v, const float* mask, void
   prm->H = H;
   prm->Nq = Nq;
   prm->Nk = Nk;
-  prm->BH = (int)BH;
-  prm->units_per_bh = (int)upb;
+  prm->BH = (int)sh.BH;
+  prm->units_per_bh = (int)sh.upb;
   prm->nkv = (Nk + 127) / 128;
   prm->num_splits = 1;
   prm->mask_heads = 1;
-  prm->num_units = (int)(BH * upb);
+  prm->num_units = (int)(sh.BH * sh.upb);
   prm->scale_log2 = (float)((double)scale * 1.4426950408889634);
   prm->timeout_ns = timeout_ns_from_env();
   prm->inject_stall = (inject && std::strcmp(inject, "stall") == 0) ? 1 : 0;
@@ -281,13 +306,23 @@ int effective_splits(int nkv, int requested) { return requested < nkv ? requeste
 
 }  // namespace
 
+// Fixed scratch of fa_fwd_split_noalloc (file scope, internal linkage): every
+// GPU that loads the library holds it until the process exits.  Host code
+// must not pass its name to a kernel (it is a host-side stand-in); the device
+// address comes from cudaGetSymbolAddress, cached per device.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[FA_NOALLOC_SCRATCH_BYTES];
+static void* g_noalloc_scratch_addr[kMaxDevices] = {};
+
 extern "C" {
 
 int fa_fwd(const void* q, const void* k, const void* v, const float* mask, void* out, float* lse,
            int B, int H, int Nq, int Nk, int D, float scale, void* stream) {
+  Shape sh;
+  int rc = validate(q, k, v, mask, out, lse, B, H, Nq, Nk, D, scale, &sh);
+  if (rc != FA_OK) return rc;
   fa::Params prm;
   DeviceState* st = nullptr;
-  const int rc = prepare(q, k, v, mask, out, lse, B, H, Nq, Nk, D, scale, &prm, &st);
+  rc = setup(q, k, v, mask, out, lse, H, Nq, Nk, D, scale, sh, &prm, &st);
   if (rc != FA_OK) return rc;
   return launch_fwd(prm, *st, D, reinterpret_cast<cudaStream_t>(stream));
 }
@@ -307,17 +342,21 @@ int fa_fwd_ex(const void* q, const void* k, const void* v, const fa_mask* mask, 
       return FA_ERR_INVALID_ARGUMENT;
   }
   const float* key_mask = kind == FA_MASK_KEY_PADDING ? static_cast<const float*>(mask->data) : nullptr;
-  fa::Params prm;
-  DeviceState* st = nullptr;
-  int rc = prepare(q, k, v, key_mask, out, lse, B, H, Nq, Nk, D, scale, &prm, &st);
+  Shape sh;
+  int rc = validate(q, k, v, key_mask, out, lse, B, H, Nq, Nk, D, scale, &sh);
   if (rc != FA_OK) return rc;
   if (full) {
     const size_t fm_bytes =
         (size_t)B * mask->heads * Nq * Nk * (kind == FA_MASK_ADDITIVE ? sizeof(float) : 1);
-    const size_t rows = (size_t)B * H * Nq;
-    if (ranges_overlap(mask->data, fm_bytes, out, rows * D * 2) ||
-        ranges_overlap(mask->data, fm_bytes, lse, rows * 4))
+    if (ranges_overlap(mask->data, fm_bytes, out, sh.q_bytes) ||
+        ranges_overlap(mask->data, fm_bytes, lse, sh.lse_bytes))
       return FA_ERR_INVALID_ARGUMENT;
+  }
+  fa::Params prm;
+  DeviceState* st = nullptr;
+  rc = setup(q, k, v, key_mask, out, lse, H, Nq, Nk, D, scale, sh, &prm, &st);
+  if (rc != FA_OK) return rc;
+  if (full) {
     prm.full_mask = mask->data;
     prm.full_mask_bool = kind == FA_MASK_BOOL;
     prm.mask_heads = mask->heads;
@@ -334,23 +373,18 @@ size_t fa_fp8_workspace_bytes(int B, int H, int Nq, int Nk, int D) {
 int fa_fwd_fp8(const void* q, const void* k, const void* v, const float* mask, void* out,
                float* lse, int B, int H, int Nq, int Nk, int D, float scale, void* workspace,
                size_t workspace_bytes, void* stream) {
+  Shape sh;
+  int rc = validate(q, k, v, mask, out, lse, B, H, Nq, Nk, D, scale, &sh);
+  if (rc != FA_OK) return rc;
   if (!workspace || !aligned16(workspace)) return FA_ERR_INVALID_ARGUMENT;
-  if (B >= 1 && H >= 1 && Nq >= 1 && Nk >= 1 && (D == 32 || D == 64 || D == 128) &&
-      workspace_bytes < fa_fp8_workspace_bytes(B, H, Nq, Nk, D))
+  const F8Layout L = f8_layout(B, H, Nq, Nk, D);
+  if (workspace_bytes < L.total) return FA_ERR_INVALID_ARGUMENT;
+  if (workspace_overlaps(workspace, L.total, q, k, v, mask, out, lse, sh))
     return FA_ERR_INVALID_ARGUMENT;
   fa::Params prm;
   DeviceState* st = nullptr;
-  int rc = prepare(q, k, v, mask, out, lse, B, H, Nq, Nk, D, scale, &prm, &st);
+  rc = setup(q, k, v, mask, out, lse, H, Nq, Nk, D, scale, sh, &prm, &st);
   if (rc != FA_OK) return rc;
-  const F8Layout L = f8_layout(B, H, Nq, Nk, D);
-  const size_t rows = (size_t)prm.BH * Nq;
-  if (ranges_overlap(workspace, L.total, q, rows * D * 2) ||
-      ranges_overlap(workspace, L.total, k, (size_t)prm.BH * Nk * D * 2) ||
-      ranges_overlap(workspace, L.total, v, (size_t)prm.BH * Nk * D * 2) ||
-      ranges_overlap(workspace, L.total, out, rows * D * 2) ||
-      ranges_overlap(workspace, L.total, lse, rows * 4) ||
-      ranges_overlap(workspace, L.total, mask, mask ? (size_t)B * Nk * 4 : 0))
-    return FA_ERR_INVALID_ARGUMENT;
   char* ws = static_cast<char*>(workspace);
   if (encode_map_f8(&prm.tm_q, ws + L.q8, prm.BH, Nq, D) != FA_OK ||
       encode_map_f8(&prm.tm_k, ws + L.k8, prm.BH, Nk, D) != FA_OK)
@@ -392,34 +426,31 @@ int fa_fwd_split(const void* q, const void* k, const void* v, const float* mask,
                  float* lse, int B, int H, int Nq, int Nk, int D, float scale, int num_splits,
                  void* workspace, size_t workspace_bytes, void* stream) {
   if (num_splits < 1) return FA_ERR_INVALID_ARGUMENT;
-  const int nkv = Nk > 0 ? (Nk + 127) / 128 : 1;
-  const int splits = effective_splits(nkv, num_splits);
+  Shape sh;
+  int rc = validate(q, k, v, mask, out, lse, B, H, Nq, Nk, D, scale, &sh);
+  if (rc != FA_OK) return rc;
+  const int splits = effective_splits((Nk + 127) / 128, num_splits);
   if (splits > 1) {
     if (!workspace || !aligned16(workspace)) return FA_ERR_INVALID_ARGUMENT;
     if (workspace_bytes < fa_split_workspace_bytes(B, H, Nq, D, splits)) return FA_ERR_INVALID_ARGUMENT;
+    if (workspace_overlaps(workspace, workspace_bytes, q, k, v, mask, out, lse, sh))
+      return FA_ERR_INVALID_ARGUMENT;
+    // Split units: checked in 64 bits before the int32 product is formed.
+    if (sh.BH * sh.upb * splits > INT_MAX) return FA_ERR_INVALID_ARGUMENT;
   }
   fa::Params prm;
   DeviceState* st = nullptr;
-  int rc = prepare(q, k, v, mask, out, lse, B, H, Nq, Nk, D, scale, &prm, &st);
+  rc = setup(q, k, v, mask, out, lse, H, Nq, Nk, D, scale, sh, &prm, &st);
   if (rc != FA_OK) return rc;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (splits == 1) return launch_fwd(prm, *st, D, s);
 
   const size_t rows = (size_t)prm.BH * Nq;
   const size_t o_bytes = align256(rows * splits * D * sizeof(float));
-  if (ranges_overlap(workspace, workspace_bytes, q, (size_t)prm.BH * Nq * D * 2) ||
-      ranges_overlap(workspace, workspace_bytes, k, (size_t)prm.BH * Nk * D * 2) ||
-      ranges_overlap(workspace, workspace_bytes, v, (size_t)prm.BH * Nk * D * 2) ||
-      ranges_overlap(workspace, workspace_bytes, out, rows * D * 2) ||
-      ranges_overlap(workspace, workspace_bytes, lse, rows * 4) ||
-      ranges_overlap(workspace, workspace_bytes, mask, mask ? (size_t)B * Nk * 4 : 0))
-    return FA_ERR_INVALID_ARGUMENT;
   prm.num_splits = splits;
-  prm.num_units *= splits;
+  prm.num_units = (int)(sh.BH * sh.upb * splits);
   prm.part_o = reinterpret_cast<float*>(workspace);
   prm.part_lse = reinterpret_cast<float*>(reinterpret_cast<char*>(workspace) + o_bytes);
-  if (prm.num_units < 0 || (long long)prm.BH * prm.units_per_bh * splits > INT_MAX)
-    return FA_ERR_INVALID_ARGUMENT;
   rc = launch_fwd(prm, *st, D, s);
   if (rc != FA_OK) return rc;
   return launch_merge(prm.part_o, prm.part_lse, prm.out, lse, splits, (long long)rows, D, s);
@@ -433,25 +464,25 @@ int fa_fwd_split(const void* q, const void* k, const void* v, const float* mask,
 // scratch is a fixed array inside this library.  A __device__ array's name in
 // host code is only a host-side stand-in, so its device address is looked up
 // with cudaGetSymbolAddress, once per device, with that device current; that
-// look-up happens on the first call on each device.
+// look-up happens on the first call on each device that uses more than one
+// key range.
 // ---------------------------------------------------------------------------
-namespace {
-__device__ __align__(256) unsigned char g_noalloc_scratch[FA_NOALLOC_SCRATCH_BYTES];
-void* g_noalloc_scratch_addr[kMaxDevices] = {};
-}  // namespace
-
 int fa_fwd_split_noalloc(const void* q, const void* k, const void* v, const float* mask, void* out,
                          float* lse, int B, int H, int Nq, int Nk, int D, float scale,
                          int num_splits, void* stream) {
-  if (num_splits < 1 || Nk < 1) return FA_ERR_INVALID_ARGUMENT;
+  // ---- validation: no CUDA call before this block passes ----
+  if (num_splits < 1) return FA_ERR_INVALID_ARGUMENT;
+  Shape sh;
+  const int rc = validate(q, k, v, mask, out, lse, B, H, Nq, Nk, D, scale, &sh);
+  if (rc != FA_OK) return rc;
   const int splits = effective_splits((Nk + 127) / 128, num_splits);
-  const size_t need = splits > 1 ? fa_split_workspace_bytes(B, H, Nq, D, splits) : 0;
-  if (splits > 1 && (need == 0 || need > (size_t)FA_NOALLOC_SCRATCH_BYTES))
-    return FA_ERR_INVALID_ARGUMENT;  // does not fit the fixed scratch (or bad sizes)
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
+  if (splits > 1 && fa_split_workspace_bytes(B, H, Nq, D, splits) > (size_t)FA_NOALLOC_SCRATCH_BYTES)
+    return FA_ERR_INVALID_ARGUMENT;  // does not fit the fixed scratch
+  // One key range needs no scratch: fa_fwd_split then launches the plain forward.
   void* scratch = nullptr;
-  {
+  if (splits > 1) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_mutex);
     if (!g_noalloc_scratch_addr[dev]) {
       void* addr = nullptr;
@@ -464,7 +495,7 @@ int fa_fwd_split_noalloc(const void* q, const void* k, const void* v, const floa
   // Every partial result the merge reads is written first by the forward, so
   // nothing in the scratch needs clearing between calls.
   return fa_fwd_split(q, k, v, mask, out, lse, B, H, Nq, Nk, D, scale, splits, scratch,
-                      (size_t)FA_NOALLOC_SCRATCH_BYTES, stream);
+                      scratch ? (size_t)FA_NOALLOC_SCRATCH_BYTES : 0, stream);
 }
 
 size_t fa_window_workspace_bytes(int B, int H, int img_h, int img_w, int D) {
@@ -482,8 +513,11 @@ int fa_fwd_window(const void* q, const void* k, const void* v, void* out, float*
     return FA_ERR_INVALID_ARGUMENT;
   if (img_h % win_h || img_w % win_w) return FA_ERR_INVALID_ARGUMENT;
   if (D != 32 && D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+  if (!std::isfinite(scale)) return FA_ERR_INVALID_ARGUMENT;
   if ((int64_t)img_h * img_w > INT_MAX) return FA_ERR_INVALID_ARGUMENT;
   if (!aligned16(workspace) || workspace_bytes < fa_window_workspace_bytes(B, H, img_h, img_w, D))
+    return FA_ERR_INVALID_ARGUMENT;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse))
     return FA_ERR_INVALID_ARGUMENT;
   const int N = img_h * img_w;
   const size_t rows = (size_t)B * H * N;
@@ -491,9 +525,7 @@ int fa_fwd_window(const void* q, const void* k, const void* v, void* out, float*
   const size_t ws_used = fa_window_workspace_bytes(B, H, img_h, img_w, D);
   if (ranges_overlap(workspace, ws_used, q, t_bytes) || ranges_overlap(workspace, ws_used, k, t_bytes) ||
       ranges_overlap(workspace, ws_used, v, t_bytes) || ranges_overlap(workspace, ws_used, out, t_bytes) ||
-      ranges_overlap(workspace, ws_used, lse, rows * 4))
-    return FA_ERR_INVALID_ARGUMENT;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse))
+      ranges_overlap(workspace, ws_used, lse, rows * 4) || ranges_overlap(out, t_bytes, lse, rows * 4))
     return FA_ERR_INVALID_ARGUMENT;
   fa::WindowGeom g{B, H, img_h, img_w, win_h, win_w, 0, 0, D, 1};
   g.shift_h = ((shift_h % img_h) + img_h) % img_h;
@@ -508,6 +540,9 @@ int fa_fwd_window(const void* q, const void* k, const void* v, void* out, float*
     while (pk > 1 && ((long long)B * nw) % pk) --pk;
     g.pack = pk;
   }
+  const long long chunks = (long long)rows * (D / 8);
+  const long long blocks = (chunks + 255) / 256;
+  if (blocks > INT_MAX) return FA_ERR_INVALID_ARGUMENT;
 
   char* ws = static_cast<char*>(workspace);
   const size_t t_al = align256(t_bytes);
@@ -516,23 +551,25 @@ int fa_fwd_window(const void* q, const void* k, const void* v, void* out, float*
   void* vw = ws + 2 * t_al;
   void* ow = ws + 3 * t_al;
   float* lw = reinterpret_cast<float*>(ws + 4 * t_al);
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // The batched problem over the gathered windows, validated like fa_fwd's.
+  const int entries = (int)(B * nw / g.pack), Ne = g.entry_tokens();
+  Shape sh;
+  int rc = validate(qw, kw, vw, nullptr, ow, lw, entries, H, Ne, Ne, D, scale, &sh);
+  if (rc != FA_OK) return rc;
 
-  const long long chunks = (long long)rows * (D / 8);
-  const long long blocks = (chunks + 255) / 256;
-  if (blocks > INT_MAX) return FA_ERR_INVALID_ARGUMENT;
-  if (std::getenv("FA_FAULT_INJECT") && std::strcmp(std::getenv("FA_FAULT_INJECT"), "launch") == 0)
-    return FA_ERR_CUDA;
+  // ---- set-up (CUDA calls, nothing enqueued yet) ----
+  fa::Params prm;
+  DeviceState* st = nullptr;
+  rc = setup(qw, kw, vw, nullptr, ow, lw, H, Ne, Ne, D, scale, sh, &prm, &st);
+  if (rc != FA_OK) return rc;
+  prm.seg = g.pack > 1 ? Nw : 0;  // each row sees its own window only
+
+  // ---- enqueue: gather, attention, scatter ----
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   fa::fa_window_gather_kernel<<<(int)blocks, 256, 0, s>>>(
       static_cast<const uint4*>(q), static_cast<const uint4*>(k), static_cast<const uint4*>(v),
       static_cast<uint4*>(qw), static_cast<uint4*>(kw), static_cast<uint4*>(vw), g, chunks);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
-  const int entries = (int)(B * nw / g.pack), Ne = g.entry_tokens();
-  fa::Params prm;
-  DeviceState* st = nullptr;
-  int rc = prepare(qw, kw, vw, nullptr, ow, lw, entries, H, Ne, Ne, D, scale, &prm, &st);
-  if (rc != FA_OK) return rc;
-  prm.seg = g.pack > 1 ? Nw : 0;  // each row sees its own window only
   rc = launch_fwd(prm, *st, D, s);
   if (rc != FA_OK) return rc;
   fa::fa_window_scatter_kernel<<<(int)blocks, 256, 0, s>>>(
