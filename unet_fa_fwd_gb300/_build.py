@@ -1,7 +1,11 @@
 """Build the CUDA library ``libfa_fwd.so`` in-tree with nvcc for sm_103a.
 
-One translation unit, static CUDA runtime, no link-time dependency on the
-driver library (the tensor-map encoder is looked up at run time).
+Four translation units (the C ABI and helper kernels in ``fa_fwd.cu``, the
+attention kernel's instantiations per head dimension in ``fa_attn_d32.cu`` /
+``fa_attn_d64.cu`` / ``fa_attn_d128.cu``) are compiled to objects in
+parallel, then linked with the static CUDA runtime; there is no link-time
+dependency on the driver library (the tensor-map encoder is looked up at run
+time).
 """
 from __future__ import annotations
 
@@ -16,7 +20,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libfa_fwd.so")
-MAIN = os.path.join(CSRC, "fa_fwd.cu")
+OBJ_DIR = os.path.join(PKG, "_build")
+UNITS = ["fa_fwd.cu", "fa_attn_d32.cu", "fa_attn_d64.cu", "fa_attn_d128.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -31,9 +36,17 @@ def sources() -> list[str]:
     return sorted(glob.glob(os.path.join(CSRC, "*"))) + [os.path.join(INCLUDE, "fa.h")]
 
 
-def build_cmd(extra: list[str] | None = None) -> list[str]:
-    return [_nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-shared", "-Xcompiler", "-fPIC",
-            "-cudart", "static", "-I", INCLUDE, "-I", CSRC, "-o", LIB, MAIN, *(extra or [])]
+def _obj(unit: str) -> str:
+    return os.path.join(OBJ_DIR, unit.replace(".cu", ".o"))
+
+
+def compile_cmd(unit: str, extra: list[str] | None = None) -> list[str]:
+    return [_nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE,
+            "-I", CSRC, "-c", "-o", _obj(unit), os.path.join(CSRC, unit), *(extra or [])]
+
+
+def link_cmd() -> list[str]:
+    return [_nvcc(), *ARCH, "-shared", "-cudart", "static", "-o", LIB, *(_obj(u) for u in UNITS)]
 
 
 def needs_build() -> bool:
@@ -43,10 +56,21 @@ def needs_build() -> bool:
     return any(os.path.getmtime(s) > t for s in sources())
 
 
+def _compile_and_link(extra: list[str] | None = None) -> int:
+    os.makedirs(OBJ_DIR, exist_ok=True)
+    procs = [subprocess.Popen(compile_cmd(u, extra)) for u in UNITS]
+    failed = [p.args[-1 - len(extra or [])] for p in procs if p.wait() != 0]
+    if failed:
+        print(f"nvcc failed: {failed}", file=sys.stderr)
+        return 1
+    return subprocess.call(link_cmd())
+
+
 def start_build(force: bool = False, extra: list[str] | None = None):
-    """Start nvcc in the background; returns a Popen, or None when up to date."""
+    """Start the build in the background (a child process that compiles the
+    units in parallel and links); returns its Popen, or None when up to date."""
     if force or needs_build():
-        return subprocess.Popen(build_cmd(extra))
+        return subprocess.Popen([sys.executable, os.path.abspath(__file__), "--force", *(extra or [])])
     return None
 
 
@@ -58,4 +82,7 @@ def build(force: bool = False, extra: list[str] | None = None) -> str:
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, extra=[a for a in sys.argv[1:] if a != "--force"]))
+    args = [a for a in sys.argv[1:] if a != "--force"]
+    if "--force" in sys.argv or needs_build():
+        sys.exit(_compile_and_link(args))
+    print(LIB)

@@ -1,5 +1,7 @@
 // fa_fwd.cu — C ABI of the attention forward (declared in include/fa.h):
-// argument validation, TMA descriptor encoding and the kernel launch.
+// argument validation, TMA descriptor encoding and the kernel launches.  The
+// attention kernel itself is compiled per head dimension in
+// fa_attn_d{32,64,128}.cu (see fa_attn_launch.h).
 //
 // The library is linked against the static CUDA runtime and reaches the
 // driver's tensor-map encoder through cudaGetDriverEntryPointByVersion, so it
@@ -11,6 +13,7 @@
 
 #include <climits>
 #include <cmath>
+#include <cstdarg>
 #include <cstdint>
 #include <cstdio>
 #include <cstdlib>
@@ -18,10 +21,16 @@
 #include <mutex>
 
 #include "fa.h"
-#include "fa_fwd_kernel.cuh"
+#include "fa_attn_launch.h"
+#include "fa_log.h"
 #include "fa_quant.cuh"
 #include "fa_window.cuh"
 #include "fa_diag.cuh"
+
+// Device status word (one per device): 0, or FA_ERR_TIMEOUT once a kernel
+// wait ran out of time.  Kernels in every translation unit receive its device
+// address in their parameters.
+__device__ int g_device_status = 0;
 
 namespace {
 
@@ -30,8 +39,9 @@ constexpr int kMaxDevices = 64;
 struct DeviceState {
   bool ready = false;
   bool supported = false;
+  int device = 0;
   int sm_count = 0;
-  bool attr_set[6] = {};  // D = 32, 64, 128; bf16 or e4m3 Q/K
+  int* status = nullptr;  // device address of g_device_status
 };
 
 std::mutex g_mutex;
@@ -71,7 +81,11 @@ int device_setup(int dev, DeviceState** out) {
       return FA_ERR_CUDA;
     }
     st.supported = (major == 10 && minor == 3);
+    st.device = dev;
     st.sm_count = sms;
+    void* status = nullptr;
+    if (cudaGetSymbolAddress(&status, g_device_status) != cudaSuccess || !status) return FA_ERR_CUDA;
+    st.status = static_cast<int*>(status);
     if (!g_encode) {
       void* fn = nullptr;
       cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
@@ -104,36 +118,13 @@ int encode_map(CUtensorMap* map, const void* base, int BH, int N, int D) {
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
 
-template <int D, bool F8>
-int launch(const fa::Params& prm, DeviceState& st, int slot, cudaStream_t stream) {
-  using C = fa::Cfg<D, F8>;
-  {
-    std::lock_guard<std::mutex> lock(g_mutex);
-    if (!st.attr_set[slot]) {
-      if (cudaFuncSetAttribute(fa::fa_fwd_kernel<D, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               C::SMEM_BYTES) != cudaSuccess)
-        return FA_ERR_CUDA;
-      // The warpgroup register split (setmaxnreg) must fit in the registers
-      // the launch reserves, or the increase would wait forever: refuse to
-      // launch a build where it does not.
-      cudaFuncAttributes fattr;
-      if (cudaFuncGetAttributes(&fattr, fa::fa_fwd_kernel<D, F8>) != cudaSuccess) return FA_ERR_CUDA;
-      if (2 * 128 * C::REGS_SOFTMAX + 128 * C::REGS_OTHER > fattr.numRegs * C::THREADS)
-        return FA_ERR_UNSUPPORTED;
-      st.attr_set[slot] = true;
-    }
-  }
-  const int grid = prm.num_units < st.sm_count ? prm.num_units : st.sm_count;
-  fa::fa_fwd_kernel<D, F8><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(prm);
-  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
-}
-
-
 int launch_merge(const float* part_o, const float* part_lse, __nv_bfloat16* out, float* lse,
                  int splits, long long rows, int D, cudaStream_t s) {
   const int rows_per_block = 256 / 32;
   const long long blocks = (rows + rows_per_block - 1) / rows_per_block;
   if (blocks > INT_MAX) return FA_ERR_INVALID_ARGUMENT;
+  fa::log_launch("fa_merge_kernel<D=%d> grid %lld x 256 threads, %d ranges, %lld rows", D, blocks,
+             splits, rows);
   switch (D) {
     case 32: fa::fa_merge_kernel<32><<<(int)blocks, 256, 0, s>>>(part_o, part_lse, out, lse, splits, rows); break;
     case 64: fa::fa_merge_kernel<64><<<(int)blocks, 256, 0, s>>>(part_o, part_lse, out, lse, splits, rows); break;
@@ -210,6 +201,9 @@ int setup(const void* q, const void* k, const void* v, const float* mask, void* 
   prm->out = reinterpret_cast<__nv_bfloat16*>(out);
   prm->lse = lse;
   prm->mask = mask;
+  // A key-padding row is read 16 bytes at a time when every batch row starts
+  // 16-byte aligned (the base is, so Nk % 4 == 0 suffices).
+  prm->mask_kind = mask ? ((Nk % 4 == 0) ? fa::kMaskF32Vec : fa::kMaskF32Scalar) : fa::kMaskNone;
   prm->H = H;
   prm->Nq = Nq;
   prm->Nk = Nk;
@@ -221,6 +215,7 @@ int setup(const void* q, const void* k, const void* v, const float* mask, void* 
   prm->num_units = (int)(sh.BH * sh.upb);
   prm->scale_log2 = (float)((double)scale * 1.4426950408889634);
   prm->timeout_ns = timeout_ns_from_env();
+  prm->status = (*st)->status;
   prm->inject_stall = (inject && std::strcmp(inject, "stall") == 0) ? 1 : 0;
   return FA_OK;
 }
@@ -228,17 +223,10 @@ int setup(const void* q, const void* k, const void* v, const float* mask, void* 
 int launch_fwd(const fa::Params& prm_in, DeviceState& st, int D, cudaStream_t s, bool f8 = false) {
   fa::Params prm = prm_in;
   fa::plan_last_wave(prm, st.sm_count);
-  if (f8) {
-    switch (D) {
-      case 32: return launch<32, true>(prm, st, 3, s);
-      case 64: return launch<64, true>(prm, st, 4, s);
-      default: return launch<128, true>(prm, st, 5, s);
-    }
-  }
   switch (D) {
-    case 32: return launch<32, false>(prm, st, 0, s);
-    case 64: return launch<64, false>(prm, st, 1, s);
-    default: return launch<128, false>(prm, st, 2, s);
+    case 32: return fa::launch_attention_d32(prm, f8, st.device, st.sm_count, s);
+    case 64: return fa::launch_attention_d64(prm, f8, st.device, st.sm_count, s);
+    default: return fa::launch_attention_d128(prm, f8, st.device, st.sm_count, s);
   }
 }
 
@@ -289,6 +277,9 @@ void launch_quant(const void* q, const void* k, char* ws, const F8Layout& L, int
       reinterpret_cast<const float*>(ws + L.partial), reinterpret_cast<float*>(ws + L.mean), BH, D,
       kF8ColsumSplits, Nk);
   const int kt = (Nk + 127) / 128, qt = (Nq + 127) / 128;
+  fa::log_launch("fa_k_colsum_kernel<D=%d> grid %d x %d; fa_k_mean_kernel grid %d; "
+             "fa_quant_rows_kernel<K> grid %d; fa_quant_rows_kernel<Q> grid %d (256 threads each)",
+             D, BH, kF8ColsumSplits, (BH * D + 255) / 256, BH * kt, BH * qt);
   fa::fa_quant_rows_kernel<D, true><<<BH * kt, 256, 0, s>>>(
       static_cast<const __nv_bfloat16*>(k), reinterpret_cast<const float*>(ws + L.mean),
       reinterpret_cast<uint8_t*>(ws + L.k8), reinterpret_cast<float*>(ws + L.k_scale), nullptr, Nk,
@@ -360,6 +351,12 @@ int fa_fwd_ex(const void* q, const void* k, const void* v, const fa_mask* mask, 
     prm.full_mask = mask->data;
     prm.full_mask_bool = kind == FA_MASK_BOOL;
     prm.mask_heads = mask->heads;
+    // 16-byte loads when every mask row starts 16-byte aligned.
+    const bool base16 = aligned16(mask->data);
+    if (kind == FA_MASK_BOOL)
+      prm.mask_kind = (base16 && Nk % 16 == 0) ? fa::kMaskU8Vec : fa::kMaskU8Scalar;
+    else
+      prm.mask_kind = (base16 && Nk % 4 == 0) ? fa::kMaskF32Vec : fa::kMaskF32Scalar;
   }
   prm.causal = causal ? 1 : 0;
   return launch_fwd(prm, *st, D, reinterpret_cast<cudaStream_t>(stream));
@@ -566,6 +563,9 @@ int fa_fwd_window(const void* q, const void* k, const void* v, void* out, float*
 
   // ---- enqueue: gather, attention, scatter ----
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  fa::log_launch("fa_window_gather_kernel / fa_window_scatter_kernel grid %lld x 256 threads; "
+             "%d batch entries of %d tokens (%d windows of %dx%d each)",
+             blocks, entries, Ne, g.pack, win_h, win_w);
   fa::fa_window_gather_kernel<<<(int)blocks, 256, 0, s>>>(
       static_cast<const uint4*>(q), static_cast<const uint4*>(k), static_cast<const uint4*>(v),
       static_cast<uint4*>(qw), static_cast<uint4*>(kw), static_cast<uint4*>(vw), g, chunks);
@@ -581,12 +581,12 @@ int fa_read_device_status(void* stream, int* status) {
   if (!status) return FA_ERR_INVALID_ARGUMENT;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   int value = 0;
-  if (cudaMemcpyFromSymbolAsync(&value, fa::g_device_status, sizeof(int), 0,
+  if (cudaMemcpyFromSymbolAsync(&value, g_device_status, sizeof(int), 0,
                                 cudaMemcpyDeviceToHost, s) != cudaSuccess)
     return FA_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return FA_ERR_CUDA;
   const int zero = 0;
-  if (cudaMemcpyToSymbolAsync(fa::g_device_status, &zero, sizeof(int), 0, cudaMemcpyHostToDevice,
+  if (cudaMemcpyToSymbolAsync(g_device_status, &zero, sizeof(int), 0, cudaMemcpyHostToDevice,
                               s) != cudaSuccess)
     return FA_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return FA_ERR_CUDA;

@@ -38,8 +38,6 @@ namespace fa {
 constexpr int kStatusTimeout = 4;  // == FA_ERR_TIMEOUT
 constexpr uint32_t kSuspendNs = 20000;  // longest sleep inside one mbarrier poll
 
-// Device status word (one per device per loaded library): 0 or a status code.
-__device__ int g_device_status = 0;
 
 // F8: Q and K are e4m3 (one byte) with per-128-row block scales and
 // S = Q K^T runs as kind::f8f6f4 MMAs; V and P stay bf16.
@@ -111,6 +109,8 @@ struct Params {  // 64-byte aligned through its CUtensorMap members
   const float* mask;   // key padding [B][Nk] or nullptr
   const void* full_mask;  // per (query, key) mask [B][mask_heads][Nq][Nk] or nullptr
   int full_mask_bool;     // 0: additive fp32; 1: uint8, nonzero = keep, 0 = -inf
+  int mask_kind;          // how the general softmax path reads mask values (kMask*): selects
+                          // the kernel instantiation
   int mask_heads;         // 1 (broadcast over heads) or H
   int causal;             // exclude key j > query i
   int seg;                // > 0: rows and keys form consecutive segments of this length
@@ -128,6 +128,7 @@ struct Params {  // 64-byte aligned through its CUtensorMap members
   const float* lse_corr;  // F8: [BH][Nq] scale * q_i . mean(K), added back to LSE
   int qtiles;             // ceil(Nq/128)
   unsigned long long timeout_ns;
+  int* status;         // device status word: set to FA_ERR_TIMEOUT when a wait runs out
   int inject_stall;    // test hook: CTA 0's producer withholds its 4th K/V tile
   int tail_start;      // units >= tail_start are single query tiles (halves of the
                        // last pair units; unsplit launches only), else == num_units
@@ -163,15 +164,20 @@ __device__ __forceinline__ Unit decode_unit(const Params& p, int u) {
     r.q0 = (p.units_per_bh - 1 - u / p.BH) * 256;
     r.nq = (r.q0 + 128 < p.Nq) ? 2 : 1;
   } else {
-    r.split = u % p.num_splits;
-    const int rest = u / p.num_splits;
+    r.split = p.num_splits == 1 ? 0 : u % p.num_splits;
+    const int rest = p.num_splits == 1 ? u : u / p.num_splits;
     r.bh = rest / p.units_per_bh;
     r.q0 = (rest % p.units_per_bh) * 256;
     r.nq = (r.q0 + 128 < p.Nq) ? 2 : 1;
   }
   // Balanced ranges: range s covers key blocks [s*nkv/S, (s+1)*nkv/S).
-  r.tile0 = (int)((long long)r.split * p.nkv / p.num_splits);
-  r.ntiles = (int)((long long)(r.split + 1) * p.nkv / p.num_splits) - r.tile0;
+  if (p.num_splits == 1) {
+    r.tile0 = 0;
+    r.ntiles = p.nkv;
+  } else {
+    r.tile0 = (int)((long long)r.split * p.nkv / p.num_splits);
+    r.ntiles = (int)((long long)(r.split + 1) * p.nkv / p.num_splits) - r.tile0;
+  }
   if (p.causal) {
     // Key blocks past the unit's last query row are fully masked: skip them
     // (causal launches use one key range, so at least one block remains).
@@ -239,7 +245,7 @@ struct Barriers {
 // (this wait ran out of time, or another one did).  Between polls the thread
 // sleeps in try_wait (woken when the phase completes).
 __device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity, Barriers* bars,
-                                             unsigned long long timeout_ns) {
+                                             unsigned long long timeout_ns, int* status) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = ptx::global_timer_ns();
   while (true) {
@@ -247,7 +253,7 @@ __device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity, Barr
     if (bars->abort_flag) return false;
     if (ptx::global_timer_ns() - t0 > timeout_ns) {
       bars->abort_flag = 1;
-      atomicCAS(&g_device_status, 0, kStatusTimeout);
+      atomicCAS(status, 0, kStatusTimeout);
       return false;
     }
   }
@@ -255,8 +261,8 @@ __device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity, Barr
 
 // Warp-uniform version: every lane waits, then the warp agrees.
 __device__ __forceinline__ bool bounded_wait_warp(uint32_t bar, uint32_t parity, Barriers* bars,
-                                                  unsigned long long timeout_ns) {
-  bool ok = bounded_wait(bar, parity, bars, timeout_ns);
+                                                  unsigned long long timeout_ns, int* status) {
+  bool ok = bounded_wait(bar, parity, bars, timeout_ns, status);
   return __all_sync(0xffffffffu, ok);
 }
 
@@ -294,7 +300,109 @@ __device__ __forceinline__ float2 exp2_fma_pipe(float2 x) {
   return make_float2(__uint_as_float(b0), __uint_as_float(b1));
 }
 
-template <int D, bool F8>
+// How the general softmax path reads additive mask values, one kind per
+// launch (chosen on the host from the mask, Nk and the alignment): none (only
+// the key-range checks), fp32 or uint8 values of one row read 16 bytes per
+// load (row starts 16-byte aligned), or one element per load.  The key-padding
+// mask [B][Nk] is a row shared by every query row of a batch entry.
+enum : int {
+  kMaskNone = 0,
+  kMaskF32Vec = 1,
+  kMaskF32Scalar = 2,
+  kMaskU8Vec = 3,
+  kMaskU8Scalar = 4,
+};
+
+// Mask values of one 16-key step of the general softmax path (keys
+// key0 .. key0 + 15 of the row `mrow`): 16 fp32 values, or 16 bytes packed
+// four to a word in w[0..3].  Every index is clamped inside the row (values
+// past Nk are never used: the key range excludes them).
+constexpr int kGenStep = 16;
+template <int MK>
+__device__ __forceinline__ void general_load(const void* mrow, int key0, int Nk,
+                                             uint32_t (&w)[kGenStep]) {
+  const float* mf = static_cast<const float*>(mrow);
+  const uint8_t* mb = static_cast<const uint8_t*>(mrow);
+  if constexpr (MK == kMaskF32Vec) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(mf + min(key0 + 4 * k, Nk - 4)));
+      w[4 * k] = v.x; w[4 * k + 1] = v.y; w[4 * k + 2] = v.z; w[4 * k + 3] = v.w;
+    }
+  } else if constexpr (MK == kMaskF32Scalar) {
+#pragma unroll
+    for (int i = 0; i < kGenStep; ++i) w[i] = __float_as_uint(__ldg(mf + min(key0 + i, Nk - 1)));
+  } else if constexpr (MK == kMaskU8Vec) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(mb + min(key0, Nk - 16)));
+    w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+  } else if constexpr (MK == kMaskU8Scalar) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      uint32_t x = 0;
+#pragma unroll
+      for (int b = 0; b < 4; ++b) x |= (uint32_t)__ldg(mb + min(key0 + 4 * k + b, Nk - 1)) << (8 * b);
+      w[k] = x;
+    }
+  }
+}
+
+// Pass 1 of the general softmax path for one key block: each of the row's
+// scores s (tensor memory, 16 columns per step) becomes the log2-domain value
+// t = s * sl2 + add * log2(e), or -inf outside the row's valid keys
+// [lo, lo + span) of the block (the Nk tail, the causal diagonal, the
+// segment of a packed window).  A uint8 mask value 0 excludes its key; an
+// fp32 value is added.  t is written back over s; the row max of t is
+// returned.  Only the first `nsteps` steps (an even number, uniform across the
+// warp) are processed: the caller guarantees that no row of the warp has a
+// valid key past them.  Neither loop branches per key (exclusion is a range
+// compare and a select); the steps run in pairs with two buffers of mask
+// values (a, b), each refilled right after its step, two steps ahead of its
+// next use.  `a` and `b` hold steps 0 and 1, loaded by the caller before S
+// was ready.
+template <int MK>
+__device__ __forceinline__ float general_pass1(uint32_t tS, const void* mrow, int kbase, int Nk,
+                                               int lo, uint32_t span, float sl2, int nsteps,
+                                               uint32_t (&a)[kGenStep], uint32_t (&b)[kGenStep]) {
+  constexpr float kLog2e = 1.4426950408889634f;
+  float mx = -INFINITY;
+  auto step = [&](int cb, uint32_t (&w)[kGenStep]) {
+    uint32_t r[kGenStep];
+    ptx::tmem_ld32x32b_x16(tS + cb, r);
+    const int d = cb - lo;
+#pragma unroll
+    for (int i = 0; i < kGenStep; ++i) {
+      float t = __uint_as_float(r[i]) * sl2;
+      bool keep = (uint32_t)(d + i) < span;
+      if constexpr (MK == kMaskF32Vec || MK == kMaskF32Scalar) {
+        t = fmaf(__uint_as_float(w[i]), kLog2e, t);
+      } else if constexpr (MK == kMaskU8Vec || MK == kMaskU8Scalar) {
+        keep = keep && ((w[i / 4] >> (8 * (i % 4))) & 0xffu) != 0u;
+      }
+      t = keep ? t : -INFINITY;
+      mx = fmaxf(mx, t);
+      r[i] = __float_as_uint(t);
+    }
+    ptx::tmem_st32x32b_x16(tS + cb, r);
+  };
+  const int end = nsteps * kGenStep;
+#pragma unroll 1
+  for (int cb = 0; cb < end; cb += 2 * kGenStep) {
+    // Each buffer is refilled as soon as its step has used it, with the keys
+    // it serves two steps later (clamped to the block: the last pair reloads
+    // its own keys, which are never used).
+    const int nb = kbase + min(cb + 2 * kGenStep, 128 - 2 * kGenStep);
+    step(cb, a);
+    general_load<MK>(mrow, nb, Nk, a);
+    step(cb + kGenStep, b);
+    general_load<MK>(mrow, nb + kGenStep, Nk, b);
+  }
+  return mx;
+}
+
+// MK: how the general softmax path reads mask values (kMask*).  Each kind is
+// its own instantiation, so a launch carries only the mask code it runs (the
+// kernel's speed is sensitive to its instruction footprint).
+template <int D, bool F8, int MK>
 __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
     fa_fwd_kernel(const __grid_constant__ Params p) {
   using C = Cfg<D, F8>;
@@ -363,7 +471,7 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
         const Unit un = decode_unit(p, u);
         const int bh = un.bh, q0 = un.q0;
         const int ntiles = un.nq;
-        ok = bounded_wait(ptx::smem_u32(&bars->q_empty), (uc & 1) ^ 1, bars, p.timeout_ns);
+        ok = bounded_wait(ptx::smem_u32(&bars->q_empty), (uc & 1) ^ 1, bars, p.timeout_ns, p.status);
         if (!ok) break;
         const uint32_t qbar = ptx::smem_u32(&bars->q_full);
         ptx::mbar_arrive_expect_tx(qbar, ntiles * C::QK_TILE_BYTES);
@@ -376,7 +484,7 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
           for (int kv = 0; kv < 2; ++kv, ++it) {
             const uint32_t s = it % C::STAGES;
             const uint32_t ph = (it / C::STAGES) & 1;
-            ok = bounded_wait(ptx::smem_u32(&bars->kv_empty[s]), ph ^ 1, bars, p.timeout_ns);
+            ok = bounded_wait(ptx::smem_u32(&bars->kv_empty[s]), ph ^ 1, bars, p.timeout_ns, p.status);
             if (!ok) break;
             const uint32_t fb = ptx::smem_u32(&bars->kv_full[s]);
             if (p.inject_stall && blockIdx.x == 0 && it == 3) {  // nothing arrives: consumers time out
@@ -484,11 +592,11 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
       };
       // Waits for each half of P_t, then issues its MMAs.
       auto issue_pv = [&](int t, uint32_t stg, bool first, uint32_t parity) -> bool {
-        if (!bounded_wait_warp(ptx::smem_u32(&bars->p_half[t]), parity, bars, p.timeout_ns))
+        if (!bounded_wait_warp(ptx::smem_u32(&bars->p_half[t]), parity, bars, p.timeout_ns, p.status))
           return false;
         ptx::tc_fence_after_sync();
         issue_pv_half(t, stg, 0, first);
-        if (!bounded_wait_warp(ptx::smem_u32(&bars->p_ready[t]), parity, bars, p.timeout_ns))
+        if (!bounded_wait_warp(ptx::smem_u32(&bars->p_ready[t]), parity, bars, p.timeout_ns, p.status))
           return false;
         ptx::tc_fence_after_sync();
         issue_pv_half(t, stg, 1, false);
@@ -497,7 +605,7 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
       // Wait until the ring's current stage is full; returns that stage.
       auto take_stage = [&](uint32_t& stg) -> bool {
         stg = stage;
-        const bool r = bounded_wait_warp(ptx::smem_u32(&bars->kv_full[stage]), phase, bars, p.timeout_ns);
+        const bool r = bounded_wait_warp(ptx::smem_u32(&bars->kv_full[stage]), phase, bars, p.timeout_ns, p.status);
         if (++stage == (uint32_t)C::STAGES) {
           stage = 0;
           phase ^= 1u;
@@ -510,7 +618,7 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
         const Unit un = decode_unit(p, u);
         const bool has1 = un.nq == 2;
         const int nkv = un.ntiles;
-        ok = bounded_wait_warp(ptx::smem_u32(&bars->q_full), uc & 1, bars, p.timeout_ns);
+        ok = bounded_wait_warp(ptx::smem_u32(&bars->q_full), uc & 1, bars, p.timeout_ns, p.status);
         if (!ok) break;
         ptx::tc_fence_after_sync();
         // Prologue: S for key block 0.
@@ -587,7 +695,6 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
     const uint32_t bar_p = ptx::smem_u32(&bars->p_ready[t]);
     const uint32_t bar_o = ptx::smem_u32(&bars->o_full[t]);
     const float scale_log2 = p.scale_log2;
-    constexpr float kLog2e = 1.4426950408889634f;
     constexpr float kRescaleThreshold = 8.0f;  // log2 units: P stays <= 2^8
     uint32_t sc = 0, oc = 0;
     bool ok = true;
@@ -600,14 +707,24 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
       const float* mask_b = p.mask ? p.mask + (size_t)(bh / p.H) * p.Nk : nullptr;
       const bool any_full_mask = p.full_mask != nullptr;  // warp-uniform
       const int tile_row0 = q0 + t * 128;                 // first query row of this tile
+      // The mask row this thread reads in the general path: the batch entry's
+      // key-padding row, or its own query row of a per-(query, key) mask (rows
+      // past Nq read row Nq - 1; their results are never stored).
+      const void* mrow = mask_b;
+      if (any_full_mask) {
+        const size_t fm_row =
+            ((size_t)(bh / p.H) * p.mask_heads + (p.mask_heads == 1 ? 0 : bh % p.H)) * p.Nq +
+            (size_t)min(qrow, p.Nq - 1);
+        mrow = static_cast<const uint8_t*>(p.full_mask) +
+               fm_row * p.Nk * (p.full_mask_bool ? 1 : sizeof(float));
+      }
+      // Keys of this row's segment (all keys when rows are not segmented).
+      const int seg_lo = p.seg > 0 ? (qrow / p.seg) * p.seg : 0;
+      const int seg_hi = p.seg > 0 ? seg_lo + p.seg : INT_MAX;
       float m = -INFINITY;  // running max of t_ij (log2 domain)
       float l = 0.f;        // running denominator relative to m
 
       for (int j = 0; j < un.ntiles; ++j) {
-        ok = bounded_wait_warp(bar_s, sc & 1, bars, p.timeout_ns);
-        if (!ok) break;
-        ++sc;
-        ptx::tc_fence_after_sync();
         const int kbase = (un.tile0 + j) * 128;
         // log2-domain multiplier of raw S; with e4m3 Q and K it carries the
         // two block scales (positive, so its sign is the sign of `scale`).
@@ -619,9 +736,38 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
         // stay in registers and the row max is taken on raw scores, scaled
         // once.  Otherwise (general path) scores are materialised in the log2
         // domain with the mask, the Nk tail, the causal diagonal and segments.
-        const bool general = (mask_b != nullptr) || any_full_mask || (kbase + 128 > p.Nk) ||
-                             !(sl2 >= 0.f) || (p.causal && kbase + 127 > tile_row0) ||
-                             p.seg > 0;
+        // A key-padding mask is classified per block (each lane checks four
+        // keys, the warp votes): all zero — the block needs no mask work; all
+        // excluded (-inf or past Nk) — the block contributes nothing.
+        bool blk_zero = false, blk_dead = false;
+        if (MK == kMaskF32Vec && mask_b != nullptr) {
+          const int k4 = kbase + 4 * (int)lane;
+          const float4 v = __ldg(reinterpret_cast<const float4*>(mask_b + min(k4, p.Nk - 4)));
+          const float e[4] = {v.x, v.y, v.z, v.w};
+          bool zero = true, dead = true;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const bool in = k4 + i < p.Nk;
+            zero = zero && in && e[i] == 0.f;
+            dead = dead && (!in || e[i] == -INFINITY);
+          }
+          blk_zero = __all_sync(0xffffffffu, zero);
+          blk_dead = __all_sync(0xffffffffu, dead);
+        }
+        const bool general = (mask_b != nullptr && !blk_zero) || any_full_mask ||
+                             (kbase + 128 > p.Nk) || !(sl2 >= 0.f) ||
+                             (p.causal && kbase + 127 > tile_row0) || p.seg > 0;
+        // The general path's first two steps of mask values are loaded while S
+        // is computed.
+        uint32_t mwa[kGenStep], mwb[kGenStep];
+        if (MK != kMaskNone && general && !blk_dead) {
+          general_load<MK>(mrow, kbase, p.Nk, mwa);
+          general_load<MK>(mrow, kbase + kGenStep, p.Nk, mwb);
+        }
+        ok = bounded_wait_warp(bar_s, sc & 1, bars, p.timeout_ns, p.status);
+        if (!ok) break;
+        ++sc;
+        ptx::tc_fence_after_sync();
         auto release = [&](int h) {
           ptx::tmem_wait_st();
           ptx::tc_fence_before_sync();
@@ -693,107 +839,51 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
           }
         } else {
           float mx;
-          // General path, compact: two rolled loops over the S block in tensor
-          // memory (this path runs on masked, causal-diagonal, Nk-tail and
-          // packed-window blocks, often enough that unrolled code would not stay
-          // in the instruction cache).  Pass 1 turns 16 scores at a time into
-          // log2-domain values with excluded pairs at -inf, keeps their max and
-          // writes them back; pass 2 (below) takes their exponentials.
-          mx = -INFINITY;
-          // This row of the per-(query, key) mask (rows past Nq read nothing).
-          const float* fmask_f = nullptr;
-          const uint8_t* fmask_b = nullptr;
-          if (any_full_mask && qrow < p.Nq) {
-            const size_t fm_row =
-                ((size_t)(bh / p.H) * p.mask_heads + (p.mask_heads == 1 ? 0 : bh % p.H)) * p.Nq +
-                (size_t)qrow;
-            if (p.full_mask_bool)
-              fmask_b = static_cast<const uint8_t*>(p.full_mask) + fm_row * p.Nk;
-            else
-              fmask_f = static_cast<const float*>(p.full_mask) + fm_row * p.Nk;
+          // General path: two rolled loops over the S block in tensor memory
+          // (this path runs on masked, causal-diagonal, Nk-tail and
+          // packed-window blocks).  Pass 1 (general_pass1) turns 16 scores at a
+          // time into log2-domain values with excluded pairs at -inf, keeps
+          // their max and writes them back; pass 2 (below) takes their
+          // exponentials.  Neither loop branches per key: a key's exclusion
+          // is a range compare and a select.
+          // The row's valid keys within this block: [lo, hi).
+          int hi = min(128, p.Nk - kbase);
+          if (p.causal) hi = min(hi, qrow - kbase + 1);
+          int lo = 0;
+          if (p.seg > 0) {
+            lo = max(0, seg_lo - kbase);
+            hi = min(hi, seg_hi - kbase);
           }
-          // Keys of this row's segment (all keys when rows are not segmented).
-          const int seg_lo = p.seg > 0 ? (qrow / p.seg) * p.seg : 0;
-          const int seg_hi = p.seg > 0 ? seg_lo + p.seg : p.Nk;
-          // Masks are read 8 keys per load: two 16-byte loads of fp32, one
-          // 8-byte load of uint8, when the 8 keys lie inside Nk and every row
-          // start is aligned (base pointer aligned and Nk a multiple of 4 / 8;
-          // the C ABI admits 4-byte-aligned fp32 and unaligned uint8 masks);
-          // scalar loads otherwise.
-          const float* madd = mask_b ? mask_b : fmask_f;  // at most one additive mask
-          const float* madd_base = p.mask ? p.mask : (p.full_mask_bool ? nullptr
-                                                      : static_cast<const float*>(p.full_mask));
-          const bool vec_f = (p.Nk & 3) == 0 && (reinterpret_cast<uintptr_t>(madd_base) & 15u) == 0;
-          const bool vec_b = (p.Nk & 7) == 0 && (reinterpret_cast<uintptr_t>(p.full_mask) & 7u) == 0;
-#pragma unroll 1
-          for (int cb = 0; cb < 128; cb += 16) {
-            uint32_t r[16];
-            ptx::tmem_ld32x32b_x16(tS + cb, r);
-            float add[16];
-            uint32_t keepbits = 0xffffu;  // bit i: key cb + i kept by the bool mask
-#pragma unroll
-            for (int i = 0; i < 16; ++i) add[i] = 0.f;
-#pragma unroll
-            for (int h = 0; h < 16; h += 8) {
-              const int key0 = kbase + cb + h;
-              const bool whole = key0 + 8 <= p.Nk;
-              if (madd) {
-                if (whole && vec_f) {
-                  const float4 a = __ldg(reinterpret_cast<const float4*>(madd + key0));
-                  const float4 b = __ldg(reinterpret_cast<const float4*>(madd + key0 + 4));
-                  add[h + 0] = a.x; add[h + 1] = a.y; add[h + 2] = a.z; add[h + 3] = a.w;
-                  add[h + 4] = b.x; add[h + 5] = b.y; add[h + 6] = b.z; add[h + 7] = b.w;
-                } else {
-#pragma unroll
-                  for (int i = 0; i < 8; ++i)
-                    if (key0 + i < p.Nk) add[h + i] = __ldg(madd + key0 + i);
-                }
-              }
-              if (fmask_b) {
-                if (whole && vec_b) {
-                  const uint2 v = __ldg(reinterpret_cast<const uint2*>(fmask_b + key0));
-#pragma unroll
-                  for (int i = 0; i < 4; ++i) {
-                    if (((v.x >> (8 * i)) & 0xffu) == 0u) keepbits &= ~(1u << (h + i));
-                    if (((v.y >> (8 * i)) & 0xffu) == 0u) keepbits &= ~(1u << (h + 4 + i));
-                  }
-                } else {
-#pragma unroll
-                  for (int i = 0; i < 8; ++i)
-                    if (key0 + i < p.Nk && __ldg(fmask_b + key0 + i) == 0)
-                      keepbits &= ~(1u << (h + i));
-                }
-              }
-            }
-            uint32_t tv_bits[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const int key = kbase + cb + i;
-              float tv = -INFINITY;
-              if (key < p.Nk && !(p.causal && key > qrow) && ((keepbits >> i) & 1u) &&
-                  key >= seg_lo && key < seg_hi)
-                tv = fmaf(add[i], kLog2e, __uint_as_float(r[i]) * sl2);
-              mx = fmaxf(mx, tv);
-              tv_bits[i] = __float_as_uint(tv);
-            }
-            ptx::tmem_st32x32b_x16(tS + cb, tv_bits);
-          }
+          const uint32_t span = hi > lo ? (uint32_t)(hi - lo) : 0u;
+          // Steps (pairs of 16 keys) that hold a valid key for some row of
+          // this warp; later columns are excluded for all 32 rows.
+          // (None when the key-padding mask excludes the whole block: P = 0
+          // and m, l are unchanged.)
+          const int hmax = __reduce_max_sync(0xffffffffu, span ? hi : 0);
+          const int nsteps = blk_dead ? 0 : min(8, 2 * ((hmax + 31) / 32));
+          mx = general_pass1<MK>(tS, mrow, kbase, p.Nk, lo, span, sl2, nsteps, mwa, mwb);
           ptx::tmem_wait_st();  // pass 2 reads these columns back
           update_max(mx);
           // Pass 2 of the general path: exponentials of the log2-domain values
           // pass 1 left in tensor memory; P (bf16 pairs) goes over the first 64
-          // columns, behind the columns still to be read.
+          // columns, behind the columns still to be read.  Columns past the
+          // steps pass 1 processed are excluded for every row: P = 0 there.
 #pragma unroll 1
           for (int cb = 0; cb < 128; cb += 32) {
-            uint32_t r[32];
-            ptx::tmem_ld32x32b_x32(tS + cb, r);
             uint32_t packed[16];
+            if (cb < nsteps * kGenStep) {
+              uint32_t r[32];
+              ptx::tmem_ld32x32b_x32(tS + cb, r);
 #pragma unroll
-            for (int c = 0; c < 32; c += 2) {
-              const float p0 = ptx::ex2(__uint_as_float(r[c]) - m_use);
-              const float p1 = ptx::ex2(__uint_as_float(r[c + 1]) - m_use);
-              lsum = __fadd2_rn(lsum, make_float2(p0, p1));
-              packed[c / 2] = ptx::pack_bf16x2(p0, p1);
+              for (int c = 0; c < 32; c += 2) {
+                const float p0 = ptx::ex2(__uint_as_float(r[c]) - m_use);
+                const float p1 = ptx::ex2(__uint_as_float(r[c + 1]) - m_use);
+                lsum = __fadd2_rn(lsum, make_float2(p0, p1));
+                packed[c / 2] = ptx::pack_bf16x2(p0, p1);
+              }
+            } else {
+#pragma unroll
+              for (int c = 0; c < 16; ++c) packed[c] = 0u;
             }
             ptx::tmem_st32x32b_x16(tS + cb / 2, packed);
             if (cb == 32 && !rescale_o) release(0);
@@ -818,7 +908,7 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
       if (!ok) break;
 
       // Epilogue: O / l -> bf16, LSE = ln2 * (m + log2 l).
-      ok = bounded_wait_warp(bar_o, oc & 1, bars, p.timeout_ns);
+      ok = bounded_wait_warp(bar_o, oc & 1, bars, p.timeout_ns, p.status);
       if (!ok) break;
       ++oc;
       ptx::tc_fence_after_sync();

@@ -139,7 +139,10 @@ __device__ __forceinline__ void mma_commit_el(uint32_t bar) {
       : "memory");
 }
 
+// Wait for this thread's earlier tcgen05.st (warp-collective, like the
+// loads and stores: the warp is reconverged first).
 __device__ __forceinline__ void tmem_wait_st() {
+  __syncwarp();
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
