@@ -213,6 +213,10 @@ int setup(const void* q, const void* k, const void* v, const float* mask, void* 
   prm->num_splits = 1;
   prm->mask_heads = 1;
   prm->num_units = (int)(sh.BH * sh.upb);
+  prm->div_upb = fa::FastDiv::make((uint32_t)sh.upb);
+  prm->div_splits = fa::FastDiv::make(1);
+  prm->div_bh = fa::FastDiv::make((uint32_t)sh.BH);
+  prm->div_h = fa::FastDiv::make((uint32_t)H);
   prm->scale_log2 = (float)((double)scale * 1.4426950408889634);
   prm->timeout_ns = timeout_ns_from_env();
   prm->status = (*st)->status;
@@ -445,6 +449,7 @@ int fa_fwd_split(const void* q, const void* k, const void* v, const float* mask,
   const size_t rows = (size_t)prm.BH * Nq;
   const size_t o_bytes = align256(rows * splits * D * sizeof(float));
   prm.num_splits = splits;
+  prm.div_splits = fa::FastDiv::make((uint32_t)splits);
   prm.num_units = (int)(sh.BH * sh.upb * splits);
   prm.part_o = reinterpret_cast<float*>(workspace);
   prm.part_lse = reinterpret_cast<float*>(reinterpret_cast<char*>(workspace) + o_bytes);

@@ -31,6 +31,7 @@
 #include <climits>
 #include <cstdint>
 
+#include "fa_fastdiv.h"
 #include "sm100_ptx.cuh"
 
 namespace fa {
@@ -100,39 +101,53 @@ struct Cfg {
   static_assert(2 * 128 * REGS_SOFTMAX + 128 * REGS_OTHER <= THREADS * 168, "register split");
 };
 
-struct Params {  // 64-byte aligned through its CUtensorMap members
-  CUtensorMap tm_q;  // [BH][Nq][D] bf16
-  CUtensorMap tm_k;  // [BH][Nk][D]
-  CUtensorMap tm_v;  // [BH][Nk][D]
+// Kernel parameters.  The scalars every role reads to decode its work units
+// come first, within the first 64 bytes, then the other scalars and pointers,
+// then the three tensor maps (64-byte aligned): a CTA's first reads of its
+// parameters miss the constant cache, and fewer distinct lines mean fewer
+// serial misses before the first copy is issued.
+struct Params {
+  // -- unit decode (first line) --
+  int num_units;       // BH * units_per_bh * num_splits
+  int tail_start;      // units >= tail_start are single query tiles (halves of the
+                       // last pair units; unsplit launches only), else == num_units
+  int units_per_bh;    // ceil(ceil(Nq/128)/2)
+  int num_splits;      // key ranges computed separately (1 = no split), <= nkv
+  int nkv;             // ceil(Nk/128): key blocks in all
+  int causal;          // exclude key j > query i
+  int BH, H, Nq, Nk;
+  int seg;             // > 0: rows and keys form consecutive segments of this length
+                       // and a row sees only keys of its own segment (packed windows)
+  int inject_stall;    // test hook: CTA 0's producer withholds its 4th K/V tile
+  FastDiv div_upb;     // division by units_per_bh
+  FastDiv div_splits;  // by num_splits
+  FastDiv div_bh;      // by BH
+  FastDiv div_h;       // by H
+  unsigned long long timeout_ns;
+  // -- softmax and epilogue --
+  float scale_log2;    // scale * log2(e)
+  int mask_kind;       // how the general softmax path reads mask values (kMask*): selects
+                       // the kernel instantiation
+  int full_mask_bool;  // 0: additive fp32; 1: uint8, nonzero = keep, 0 = -inf
+  int mask_heads;      // 1 (broadcast over heads) or H
+  int qtiles;          // ceil(Nq/128)
+  int* status;         // device status word: set to FA_ERR_TIMEOUT when a wait runs out
   __nv_bfloat16* out;  // [BH][Nq][D]
   float* lse;          // [BH][Nq]
   const float* mask;   // key padding [B][Nk] or nullptr
   const void* full_mask;  // per (query, key) mask [B][mask_heads][Nq][Nk] or nullptr
-  int full_mask_bool;     // 0: additive fp32; 1: uint8, nonzero = keep, 0 = -inf
-  int mask_kind;          // how the general softmax path reads mask values (kMask*): selects
-                          // the kernel instantiation
-  int mask_heads;         // 1 (broadcast over heads) or H
-  int causal;             // exclude key j > query i
-  int seg;                // > 0: rows and keys form consecutive segments of this length
-                          // and a row sees only keys of its own segment (packed windows)
-  int H, Nq, Nk, BH;
-  int num_units;       // BH * units_per_bh * num_splits
-  int units_per_bh;    // ceil(ceil(Nq/128)/2)
-  int nkv;             // ceil(Nk/128): key blocks in all
-  int num_splits;      // key ranges computed separately (1 = no split), <= nkv
   float* part_o;       // split mode: fp32 [num_splits][BH][Nq][D] partial O (else nullptr)
   float* part_lse;     // split mode: fp32 [num_splits][BH][Nq] partial LSE
-  float scale_log2;    // scale * log2(e)
   const float* q_scale;   // F8: [BH][ceil(Nq/128)] e4m3 block scale of Q
   const float* k_scale;   // F8: [BH][nkv] e4m3 block scale of the smoothed K
   const float* lse_corr;  // F8: [BH][Nq] scale * q_i . mean(K), added back to LSE
-  int qtiles;             // ceil(Nq/128)
-  unsigned long long timeout_ns;
-  int* status;         // device status word: set to FA_ERR_TIMEOUT when a wait runs out
-  int inject_stall;    // test hook: CTA 0's producer withholds its 4th K/V tile
-  int tail_start;      // units >= tail_start are single query tiles (halves of the
-                       // last pair units; unsplit launches only), else == num_units
+  // -- TMA descriptors (each 64-byte aligned) --
+  CUtensorMap tm_q;  // [BH][Nq][D] bf16 (e4m3 for the F8 kernel)
+  CUtensorMap tm_k;  // [BH][Nk][D]
+  CUtensorMap tm_v;  // [BH][Nk][D]
 };
+static_assert(sizeof(Params) <= 4096, "kernel parameter space");
+
 
 // One work unit: nq query tiles (256 rows, or 128 at the Nq tail and in the
 // last wave) of one (b, h) against one range of key blocks.
@@ -147,34 +162,42 @@ struct Unit {
 // shorter.
 __device__ __forceinline__ Unit decode_unit(const Params& p, int u) {
   Unit r;
+  const uint32_t upb = (uint32_t)p.units_per_bh;
   if (u >= p.tail_start) {
-    const int v = u - p.tail_start;
-    const int pair = p.tail_start + (v >> 1);  // unsplit launch: unit == pair index
+    const uint32_t v = (uint32_t)(u - p.tail_start);
+    const uint32_t pair = (uint32_t)p.tail_start + (v >> 1);  // unsplit launch: unit == pair index
+    const uint32_t bh = p.div_upb.div(pair);
     r.split = 0;
-    r.bh = pair / p.units_per_bh;
-    r.q0 = (pair % p.units_per_bh) * 256 + (v & 1) * 128;
+    r.bh = (int)bh;
+    r.q0 = (int)(pair - bh * upb) * 256 + (int)(v & 1) * 128;
     r.nq = 1;
   } else if (p.causal) {
     // Causal (one key range): a pair's work grows with its query position, so
     // units run heaviest first across all heads (pair index descending, heads
     // inner); with the round-robin assignment this keeps the CTAs' totals
     // within a few percent, and the units of a head still start together.
+    const uint32_t k = p.div_bh.div((uint32_t)u);
     r.split = 0;
-    r.bh = u % p.BH;
-    r.q0 = (p.units_per_bh - 1 - u / p.BH) * 256;
+    r.bh = u - (int)k * p.BH;
+    r.q0 = (int)(upb - 1 - k) * 256;
     r.nq = (r.q0 + 128 < p.Nq) ? 2 : 1;
   } else {
-    r.split = p.num_splits == 1 ? 0 : u % p.num_splits;
-    const int rest = p.num_splits == 1 ? u : u / p.num_splits;
-    r.bh = rest / p.units_per_bh;
-    r.q0 = (rest % p.units_per_bh) * 256;
+    uint32_t rest = (uint32_t)u;
+    r.split = 0;
+    if (p.num_splits > 1) {
+      rest = p.div_splits.div((uint32_t)u);
+      r.split = u - (int)rest * p.num_splits;
+    }
+    const uint32_t bh = p.div_upb.div(rest);
+    r.bh = (int)bh;
+    r.q0 = (int)(rest - bh * upb) * 256;
     r.nq = (r.q0 + 128 < p.Nq) ? 2 : 1;
   }
-  // Balanced ranges: range s covers key blocks [s*nkv/S, (s+1)*nkv/S).
   if (p.num_splits == 1) {
     r.tile0 = 0;
     r.ntiles = p.nkv;
   } else {
+    // Balanced ranges: range s covers key blocks [s*nkv/S, (s+1)*nkv/S).
     r.tile0 = (int)((long long)r.split * p.nkv / p.num_splits);
     r.ntiles = (int)((long long)(r.split + 1) * p.nkv / p.num_splits) - r.tile0;
   }
@@ -704,7 +727,8 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
       const int bh = un.bh, q0 = un.q0;
       if (t == 1 && un.nq < 2) continue;
       const int qrow = q0 + t * 128 + row;
-      const float* mask_b = p.mask ? p.mask + (size_t)(bh / p.H) * p.Nk : nullptr;
+      const int b_idx = (int)p.div_h.div((uint32_t)bh);  // batch entry of this head
+      const float* mask_b = p.mask ? p.mask + (size_t)b_idx * p.Nk : nullptr;
       const bool any_full_mask = p.full_mask != nullptr;  // warp-uniform
       const int tile_row0 = q0 + t * 128;                 // first query row of this tile
       // The mask row this thread reads in the general path: the batch entry's
@@ -713,7 +737,7 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
       const void* mrow = mask_b;
       if (any_full_mask) {
         const size_t fm_row =
-            ((size_t)(bh / p.H) * p.mask_heads + (p.mask_heads == 1 ? 0 : bh % p.H)) * p.Nq +
+            ((size_t)b_idx * p.mask_heads + (p.mask_heads == 1 ? 0 : bh - b_idx * p.H)) * p.Nq +
             (size_t)min(qrow, p.Nq - 1);
         mrow = static_cast<const uint8_t*>(p.full_mask) +
                fm_row * p.Nk * (p.full_mask_bool ? 1 : sizeof(float));
@@ -736,14 +760,32 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
         // stay in registers and the row max is taken on raw scores, scaled
         // once.  Otherwise (general path) scores are materialised in the log2
         // domain with the mask, the Nk tail, the causal diagonal and segments.
+        // Blocks that need per-key work in the softmax (apart from a
+        // key-padding mask, decided below once its values have arrived).
+        const bool general_fixed = any_full_mask || (kbase + 128 > p.Nk) || !(sl2 >= 0.f) ||
+                                   (p.causal && kbase + 127 > tile_row0) || p.seg > 0;
+        // Loads issued before S is ready, so that their latency overlaps the
+        // wait: the key-padding values this lane classifies (four keys) and
+        // the general path's first two steps of mask values.
+        float4 kv4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        const int k4 = kbase + 4 * (int)lane;
+        if (MK == kMaskF32Vec && mask_b != nullptr)
+          kv4 = __ldg(reinterpret_cast<const float4*>(mask_b + min(k4, p.Nk - 4)));
+        uint32_t mwa[kGenStep], mwb[kGenStep];
+        if (MK != kMaskNone && (general_fixed || mask_b != nullptr)) {
+          general_load<MK>(mrow, kbase, p.Nk, mwa);
+          general_load<MK>(mrow, kbase + kGenStep, p.Nk, mwb);
+        }
+        ok = bounded_wait_warp(bar_s, sc & 1, bars, p.timeout_ns, p.status);
+        if (!ok) break;
+        ++sc;
+        ptx::tc_fence_after_sync();
         // A key-padding mask is classified per block (each lane checks four
         // keys, the warp votes): all zero — the block needs no mask work; all
         // excluded (-inf or past Nk) — the block contributes nothing.
         bool blk_zero = false, blk_dead = false;
         if (MK == kMaskF32Vec && mask_b != nullptr) {
-          const int k4 = kbase + 4 * (int)lane;
-          const float4 v = __ldg(reinterpret_cast<const float4*>(mask_b + min(k4, p.Nk - 4)));
-          const float e[4] = {v.x, v.y, v.z, v.w};
+          const float e[4] = {kv4.x, kv4.y, kv4.z, kv4.w};
           bool zero = true, dead = true;
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
@@ -754,20 +796,7 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
           blk_zero = __all_sync(0xffffffffu, zero);
           blk_dead = __all_sync(0xffffffffu, dead);
         }
-        const bool general = (mask_b != nullptr && !blk_zero) || any_full_mask ||
-                             (kbase + 128 > p.Nk) || !(sl2 >= 0.f) ||
-                             (p.causal && kbase + 127 > tile_row0) || p.seg > 0;
-        // The general path's first two steps of mask values are loaded while S
-        // is computed.
-        uint32_t mwa[kGenStep], mwb[kGenStep];
-        if (MK != kMaskNone && general && !blk_dead) {
-          general_load<MK>(mrow, kbase, p.Nk, mwa);
-          general_load<MK>(mrow, kbase + kGenStep, p.Nk, mwb);
-        }
-        ok = bounded_wait_warp(bar_s, sc & 1, bars, p.timeout_ns, p.status);
-        if (!ok) break;
-        ++sc;
-        ptx::tc_fence_after_sync();
+        const bool general = general_fixed || (mask_b != nullptr && !blk_zero);
         auto release = [&](int h) {
           ptx::tmem_wait_st();
           ptx::tc_fence_before_sync();
