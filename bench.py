@@ -3,16 +3,24 @@
 the fp64 CPU oracle.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl native|reference]
+                    [--variant fwd|fp8|causal|key_mask|additive_mask|bool_mask|window]
 
 A step is one attention forward (one kernel launch) over the whole workload,
-inputs resident in device memory.  Default workload: FLUX 2048² joint
-attention, B1 H24 N16896 D128 bf16 (Q/K/V 311 MB, larger than the 129 MB L2,
-so no flush is needed between steps).  Prints one JSON line on rank 0.
+inputs resident in device memory.  Default workload: HunyuanVideo 720p
+attention, B1 H24 N119056 D128 bf16 — the largest of the page configurations
+that fits one GPU (Q/K/V 2.2 GB, far larger than the 129 MB L2, so no flush is
+needed between steps).  FLUX 2048² (B1 H24 N16896 D128) and the smaller
+configurations are reported under "also".  Prints one JSON line on rank 0.
 
 N > 1 (under torchrun) runs one independent replica per GPU — the path has no
 exchange step — and reports the whole-job throughput (weak scaling).
 ``--impl reference`` times the CPU oracle instead, on a bounded sample of the
-same workload.
+same workload.  ``--variant`` times another entry point as the step (for
+profiling one path alone; the end-to-end leg and the "also" blocks are then
+skipped): the FP8 Q K^T forward, causal attention, a key-padding mask (last
+quarter of the keys excluded), a per-(query, key) additive fp32 or boolean mask
+(broadcast over heads), or 8x8 window attention on a 64x64 token grid (the
+workload must have 4096 tokens).
 """
 from __future__ import annotations
 
@@ -36,7 +44,8 @@ KERNEL_NAME = "fa_fwd_kernel"
 
 # --------------------------------------------------------------------- helpers
 
-KERNEL_FILES = ("fa_fwd_kernel.cuh", "sm100_ptx.cuh", "tmem_ldst.inc", "mma_batch.inc")
+KERNEL_FILES = ("fa_fwd_kernel.cuh", "fa_attn_impl.cuh", "fa_fastdiv.h", "sm100_ptx.cuh",
+                "tmem_ldst.inc", "mma_batch.inc")
 
 
 def kernel_source_hash() -> str:
@@ -222,8 +231,62 @@ def bench_native(args, world, rank, local):
         0 if mask is None else mask.numel() * 4)
     stream = torch.cuda.current_stream(device)
 
-    def step():
-        fa.fa_fwd(q, k, v, mask, out, lse, scale=inp["scale"], stream=stream)
+    variant = args.variant
+    if variant == "fwd":
+        def step():
+            fa.fa_fwd(q, k, v, mask, out, lse, scale=inp["scale"], stream=stream)
+    elif variant == "fp8":
+        ws8v = torch.empty(fa.fp8_workspace_bytes(B, H, Nq, Nk, D), dtype=torch.uint8, device=device)
+
+        def step():
+            fa.fa_fwd_fp8(q, k, v, mask, out, lse, ws8v, scale=inp["scale"], stream=stream)
+    elif variant == "causal":
+        kept = Nq * (Nq + 1) // 2 if Nq <= Nk else Nk * (Nk + 1) // 2 + (Nq - Nk) * Nk
+        flops = 4.0 * B * H * D * kept
+
+        def step():
+            fa.fa_fwd_ex(q, k, v, out, lse, causal=True, scale=inp["scale"], stream=stream)
+    elif variant == "key_mask":
+        kmask = torch.zeros((B, Nk), dtype=torch.float32, device=device)
+        kmask[:, Nk - Nk // 4:] = float("-inf")
+        in_bytes += kmask.numel() * 4
+
+        def step():
+            fa.fa_fwd_ex(q, k, v, out, lse, key_mask=kmask, scale=inp["scale"], stream=stream)
+    elif variant in ("additive_mask", "bool_mask"):
+        g = torch.Generator(device=device).manual_seed(2024)
+        if variant == "additive_mask":
+            fmask = torch.randn((B, 1, Nq, Nk), generator=g, device=device, dtype=torch.float32)
+        else:
+            fmask = torch.rand((B, 1, Nq, Nk), generator=g, device=device) > 0.1
+        in_bytes += fmask.numel() * fmask.element_size()
+
+        def step():
+            fa.fa_fwd_ex(q, k, v, out, lse, full_mask=fmask, scale=inp["scale"], stream=stream)
+    elif variant == "window":
+        if Nq != 4096 or Nk != 4096:
+            raise SystemExit("--variant window needs a 4096-token workload (64x64 grid)")
+        flops = 4.0 * B * H * Nq * 64 * D
+
+        def step():
+            fa.fwd_window(q, k, v, 64, 64, 8, 8, 0, 0, scale=inp["scale"], stream=stream)
+    else:
+        raise SystemExit(f"unknown variant {variant}")
+
+    def time_steps(fn, n):
+        """Mean device time (ms) of n back-to-back calls after 2 warm-up calls."""
+        for _ in range(2):
+            fn()
+        torch.cuda.synchronize(device)
+        t0_, t1_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0_.record(stream)
+        for _ in range(n):
+            fn()
+        t1_.record(stream)
+        torch.cuda.synchronize(device)
+        if fa.read_device_status(stream) != 0:
+            raise RuntimeError("kernel wait timed out")
+        return t0_.elapsed_time(t1_) / n
 
     for _ in range(args.warmup):
         step()
@@ -260,8 +323,11 @@ def bench_native(args, world, rank, local):
     # ---- end to end: pinned host inputs -> device -> fa_fwd -> host outputs ----
     # Every step uploads its Q/K/V (and mask) from pinned host memory, runs the
     # forward through the C ABI and downloads O and LSE.  Two buffer sets and
-    # three streams let step i+1's upload and step i-1's download overlap step
-    # i's kernel (events keep each buffer's writes after its previous reads).
+    # four streams (Q upload, K/V upload, compute, download) let step i+1's
+    # uploads and step i-1's download overlap step i's kernel (events keep each
+    # buffer's writes after its previous reads).
+    if variant != "fwd":
+        args.also = False
     hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
     hmask = None if mask is None else mask.cpu().pin_memory()
     nbuf = 2
@@ -270,29 +336,46 @@ def bench_native(args, world, rank, local):
     douts = [(torch.empty_like(out), torch.empty_like(lse)) for _ in range(nbuf)]
     houts = [(torch.empty(out.shape, dtype=out.dtype, pin_memory=True),
               torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)) for _ in range(nbuf)]
-    s_in, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    s_in, s_in2, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device), torch.cuda.Stream(device)
     ev = lambda: torch.cuda.Event()
+    tev = lambda: torch.cuda.Event(enable_timing=True)
     in_done = [ev() for _ in range(nbuf)]
+    in_done2 = [ev() for _ in range(nbuf)]
+    up_events = []   # (start, end of Q, end of K/V) per timed step
     used = [ev() for _ in range(nbuf)]
     out_done = [ev() for _ in range(nbuf)]
     for i in range(nbuf):   # every buffer starts free
         used[i].record(stream)
         out_done[i].record(stream)
 
-    def e2e_step(i):
+    def e2e_step(i, timed=False):
         b = i % nbuf
         dq, dk, dv, dm = dins[b]
         do, dl = douts[b]
         ho, hl = houts[b]
+        marks = (tev(), tev(), tev()) if timed else None
         with torch.cuda.stream(s_in):
             s_in.wait_event(used[b])
+            s_in2.wait_event(used[b])
+            if timed:
+                marks[0].record(s_in)
+                s_in2.wait_event(marks[0])
             dq.copy_(hq, non_blocking=True)
-            dk.copy_(hk, non_blocking=True)
-            dv.copy_(hv, non_blocking=True)
             if dm is not None:
                 dm.copy_(hmask, non_blocking=True)
             in_done[b].record(s_in)
+            if timed:
+                marks[1].record(s_in)
+        with torch.cuda.stream(s_in2):
+            dk.copy_(hk, non_blocking=True)
+            dv.copy_(hv, non_blocking=True)
+            in_done2[b].record(s_in2)
+            if timed:
+                marks[2].record(s_in2)
+        if timed:
+            up_events.append(marks)
         stream.wait_event(in_done[b])
+        stream.wait_event(in_done2[b])
         stream.wait_event(out_done[b])
         fa.fa_fwd(dq, dk, dv, dm, do, dl, scale=inp["scale"], stream=stream)
         used[b].record(stream)
@@ -302,47 +385,59 @@ def bench_native(args, world, rank, local):
             hl.copy_(dl, non_blocking=True)
             out_done[b].record(s_out)
 
-    e2e_steps = max(5, args.steps // 20)
-    for i in range(2):
-        e2e_step(i)
-    torch.cuda.synchronize(device)
-    if world > 1:
-        dist.barrier()
-    t0 = time.perf_counter()
-    for i in range(e2e_steps):
-        e2e_step(i)
-    torch.cuda.synchronize(device)
-    e2e_secs = max_over_ranks(time.perf_counter() - t0, device=device)
-    e2e_tflops = whole_job_throughput(flops * e2e_steps, world, e2e_secs) / 1e12
+    e2e_steps = max(5, args.steps // 20) if variant == "fwd" else 0
+    e2e_secs = 0.0
+    if e2e_steps:
+        for i in range(2):
+            e2e_step(i)
+        torch.cuda.synchronize(device)
+        if world > 1:
+            dist.barrier()
+        t0 = time.perf_counter()
+        for i in range(e2e_steps):
+            e2e_step(i, timed=True)
+        torch.cuda.synchronize(device)
+        e2e_secs = max_over_ranks(time.perf_counter() - t0, device=device)
+    # achieved host-to-device rate: bytes of one step's uploads over the time
+    # from their start to the later of the two streams' ends (median over steps)
+    up_ms = [max(m0.elapsed_time(m1), m0.elapsed_time(m2)) for m0, m1, m2 in up_events]
+    h2d_gbs = in_bytes / (statistics.median(up_ms) * 1e6) if up_ms else 0.0
+    e2e_tflops = (whole_job_throughput(flops * e2e_steps, world, e2e_secs) / 1e12
+                  if e2e_steps else 0.0)
     out_bytes = out.numel() * 2 + lse.numel() * 4
     del dins, douts
 
-    # ---- secondary workload: HunyuanVideo 720p (few steps) ----
+    # ---- the other large workload (few steps each), bf16 and FP8 Q K^T ----
     also = {}
-    if args.also and rank == 0 and args.workload != "hunyuan_720p":
+    if args.also and rank == 0:
         del hq, hk, hv, houts
-        hw = workloads.make_inputs("hunyuan_720p", device=device)
+        other = "flux_2048" if args.workload != "flux_2048" else "hunyuan_720p"
+        hw = workloads.make_inputs(other, device=device)
         hB, hH, hNq, hNk, hD = hw["shape"]
         hoAll = torch.empty_like(hw["q"])
         hl = torch.empty((hB, hH, hNq), dtype=torch.float32, device=device)
-        for _ in range(2):
-            fa.fa_fwd(hw["q"], hw["k"], hw["v"], None, hoAll, hl, scale=hw["scale"], stream=stream)
-        torch.cuda.synchronize(device)
-        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        n_h = 5
-        a0.record(stream)
-        for _ in range(n_h):
-            fa.fa_fwd(hw["q"], hw["k"], hw["v"], None, hoAll, hl, scale=hw["scale"], stream=stream)
-        a1.record(stream)
-        torch.cuda.synchronize(device)
-        hms = a0.elapsed_time(a1) / n_h
         hfl = accounting.attention_flops(hB, hH, hNq, hNk, hD)
-        also["hunyuan_720p"] = {"ms_per_step": round(hms, 3), "tflops": round(hfl / hms / 1e9, 1),
-                                "steps": n_h}
-        del hw, hoAll, hl
+        n_h = 20 if other == "flux_2048" else 5
+        with ClockSampler(local) as hclocks:
+            hms = time_steps(lambda: fa.fa_fwd(hw["q"], hw["k"], hw["v"], None, hoAll, hl,
+                                               scale=hw["scale"], stream=stream), n_h)
+        ws8o = torch.empty(fa.fp8_workspace_bytes(hB, hH, hNq, hNk, hD), dtype=torch.uint8,
+                           device=device)
+        hms8 = time_steps(lambda: fa.fa_fwd_fp8(hw["q"], hw["k"], hw["v"], None, hoAll, hl, ws8o,
+                                                scale=hw["scale"], stream=stream), n_h)
+        also[other] = {"ms_per_step": round(hms, 4), "tflops": round(hfl / hms / 1e9, 1),
+                       "steps": n_h, "clocks": hclocks.summary(),
+                       "fp8_qk": {"ms_per_step": round(hms8, 4),
+                                  "tflops": round(hfl / hms8 / 1e9, 1),
+                                  "speedup_vs_bf16": round(hms / hms8, 3),
+                                  "note": "pre-pass included; bf16-equivalent FLOPs"}}
+        del hw, hoAll, hl, ws8o
 
     # ---- the page's smaller configurations, each launch timed alone after an L2 flush ----
     if args.also and rank == 0:
+        # the long loops above leave the GPU at its power cap; idle briefly so the
+        # short launches below run at the clocks a cold start sees
+        time.sleep(3.0)
         flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=device)  # > 129 MB L2
         hbm = float(read_peaks()[0].get("hbm_gbs", 6671.5))
         small = {}
@@ -462,6 +557,7 @@ def bench_native(args, world, rank, local):
         ms8 = f0.elapsed_time(f1) / n8
         also["fp8_qk"] = {"workload": args.workload, "ms_per_step": round(ms8, 4),
                           "tflops": round(flops / ms8 / 1e9, 1), "steps": n8,
+                          "speedup_vs_bf16": round(ms_per_step / ms8, 3),
                           "note": "e4m3 Q K^T with K mean smoothing, bf16 P V; "
                                   "bf16-equivalent attention FLOPs; quantisation pre-pass timed"}
         del ws8
@@ -535,17 +631,20 @@ def bench_native(args, world, rank, local):
             "vs_baseline": None,
             "dtype": "bf16",
             "data": "synthetic",
-            "config": {"workload": args.workload, "B": B, "H": H, "Nq": Nq, "Nk": Nk, "D": D,
+            "config": {"workload": args.workload, "variant": variant, "B": B, "H": H, "Nq": Nq,
+                       "Nk": Nk, "D": D,
                        "masked": mask is not None, "parallelism": f"replicas{world}",
                        "l2": f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB of Q/K/V per step)"},
             "pct_of_peak": round(100.0 * kernel_tflops / peak, 2),
             "step_ms": {"median": round(statistics.median(step_ms), 4),
                         "min": round(min(step_ms), 4), "max": round(max(step_ms), 4)},
             "clocks": clock_summary,
-            "e2e": {"value": round(e2e_tflops, 2), "unit": "TFLOP/s",
-                    "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": out_bytes,
-                    "steps": e2e_steps, "overlap": "double-buffered: upload i+1 / download i-1 "
-                                                   "overlap kernel i on separate streams"},
+            "e2e": ({"value": round(e2e_tflops, 2), "unit": "TFLOP/s",
+                     "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": out_bytes,
+                     "steps": e2e_steps, "h2d_gbs": round(h2d_gbs, 1),
+                     "overlap": "double-buffered: upload i+1 (Q on one copy stream, K/V on "
+                                "another) / download i-1 overlap kernel i"}
+                    if e2e_steps else None),
             "gpu_launches": args.steps,
             "roofline": {"bound": "tensor", "achieved": round(kernel_tflops, 2), "peak": peak,
                          "unit": "TFLOP/s", "frac": round(kernel_tflops / peak, 4),
@@ -609,10 +708,12 @@ def bench_reference(args, world, rank, local):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=400)
-    ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", default="flux_2048")
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="hunyuan_720p")
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--variant", default="fwd",
+                    choices=["fwd", "fp8", "causal", "key_mask", "additive_mask", "bool_mask", "window"])
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--ref-budget", type=float, default=90.0, help="seconds of oracle work, reference arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
