@@ -221,7 +221,7 @@ def bench_native(args, world, rank, local):
     fa.load_library()
 
     w = workloads.WORKLOADS[args.workload]
-    inp = workloads.make_inputs(w, device=device)
+    inp = workloads.make_inputs(w, device=device, H=args.heads)
     B, H, Nq, Nk, D = inp["shape"]
     q, k, v, mask = inp["q"], inp["k"], inp["v"], inp["mask"]
     out = torch.empty_like(q)
@@ -631,7 +631,8 @@ def bench_native(args, world, rank, local):
             "vs_baseline": None,
             "dtype": "bf16",
             "data": "synthetic",
-            "config": {"workload": args.workload, "variant": variant, "B": B, "H": H, "Nq": Nq,
+            "config": {"workload": args.workload + ("" if args.heads is None else f" (H {H})"),
+                       "variant": variant, "B": B, "H": H, "Nq": Nq,
                        "Nk": Nk, "D": D,
                        "masked": mask is not None, "parallelism": f"replicas{world}",
                        "l2": f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB of Q/K/V per step)"},
@@ -712,6 +713,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="hunyuan_720p")
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--heads", type=int, default=None,
+                    help="override the workload's head count (smaller cases for profiling)")
     ap.add_argument("--variant", default="fwd",
                     choices=["fwd", "fp8", "causal", "key_mask", "additive_mask", "bool_mask", "window"])
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
