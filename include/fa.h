@@ -35,7 +35,9 @@ typedef enum {
     FA_ERR_INVALID_ARGUMENT = 1, /* NULL pointer, bad size, misaligned or overlapping buffer, non-finite scale */
     FA_ERR_UNSUPPORTED = 2,      /* head dimension D not in {32, 64, 128}; device not sm_103 */
     FA_ERR_CUDA = 3,             /* a CUDA runtime/driver call failed (launch, attribute, tensor map) */
-    FA_ERR_TIMEOUT = 4           /* a kernel wait ran past its time limit (read with fa_read_device_status) */
+    FA_ERR_TIMEOUT = 4,          /* a kernel wait ran past its time limit (read with fa_read_device_status) */
+    FA_ERR_DEBUG_CHECK = 5       /* debug builds: a device-side bounds or schedule check failed
+                                    (read with fa_read_device_status; details: fa_debug_report) */
 } fa_status;
 
 /*
@@ -260,6 +262,26 @@ int fa_read_device_status(void* stream, int* status);
  * SMs) or FA_ERR_CUDA.
  */
 int fa_measure_ex2_rate(void* stream, double* ex2_per_clock_per_sm);
+
+/*
+ * Debug build (libfa_fwd_debug.so, compiled with FA_DEBUG; no counterpart on
+ * the pages): every kernel checks its unit schedule and the index of every
+ * global-memory access before using it.  A failed check skips the access,
+ * records the first violation, sets FA_ERR_DEBUG_CHECK in the device status
+ * word and makes its CTA drain and exit as after a wait timeout; nothing traps.
+ * It stands in for a memory checker where none can run.
+ *
+ * fa_debug_build — 1 in the debug build, 0 in the release build.
+ *
+ * fa_debug_report — synchronise `stream`, copy the first recorded violation
+ *   to record[8] and clear it: {check id (0 = none; 1 unit schedule, 2
+ *   producer/MMA unit mismatch, 3 mask row, 4 e4m3 scale index, 5 output
+ *   store), CTA, thread, value a, value b, 0, 0, number of failed checks}.
+ *   The release build writes zeros.  Returns FA_OK, FA_ERR_INVALID_ARGUMENT
+ *   (record NULL) or FA_ERR_CUDA.
+ */
+int fa_debug_build(void);
+int fa_debug_report(void* stream, int* record);
 
 /* Human-readable name of a status code (static storage; never NULL). */
 const char* fa_status_string(int status);

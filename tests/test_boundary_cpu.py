@@ -37,10 +37,23 @@ def test_exports_every_declared_symbol(lib):
         assert hasattr(raw, n), n
 
 
+def test_debug_library_exports_the_same_symbols(lib):
+    """The debug build (device-side checks) exports every declared function too,
+    and each library reports which build it is."""
+    names = _declared()
+    dbg = ctypes.CDLL(_build.LIB_DEBUG)
+    for n in names:
+        assert hasattr(dbg, n), n
+    rel = ctypes.CDLL(_build.LIB)
+    assert rel.fa_debug_build() == 0 and dbg.fa_debug_build() == 1
+    assert dbg.fa_debug_report(None, None) == 1     # FA_ERR_INVALID_ARGUMENT, no CUDA call
+
+
 def test_strings(lib):
     assert fa.version().startswith("unet_fa_fwd_gb300")
     assert fa.status_string(0) == "FA_OK"
     assert fa.status_string(4) == "FA_ERR_TIMEOUT"
+    assert fa.status_string(5) == "FA_ERR_DEBUG_CHECK"
     assert fa.status_string(99) == "FA_ERR_UNKNOWN"
 
 

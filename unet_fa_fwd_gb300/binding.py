@@ -20,6 +20,7 @@ FA_ERR_INVALID_ARGUMENT = 1
 FA_ERR_UNSUPPORTED = 2
 FA_ERR_CUDA = 3
 FA_ERR_TIMEOUT = 4
+FA_ERR_DEBUG_CHECK = 5
 
 FA_MASK_NONE = 0
 FA_MASK_KEY_PADDING = 1
@@ -36,7 +37,9 @@ class FaMask(ctypes.Structure):
 
 
 def library_path() -> str:
-    return _build.LIB
+    """The release library, or with FA_DEBUG=1 in the environment the debug build
+    (device-side bounds and schedule checks; see fa_debug_report)."""
+    return _build.LIB_DEBUG if os.environ.get("FA_DEBUG") == "1" else _build.LIB
 
 
 def load_library() -> ctypes.CDLL:
@@ -81,6 +84,10 @@ def load_library() -> ctypes.CDLL:
             lib.fa_status_string.restype = ctypes.c_char_p
             lib.fa_version.argtypes = []
             lib.fa_version.restype = ctypes.c_char_p
+            lib.fa_debug_build.argtypes = []
+            lib.fa_debug_build.restype = i32
+            lib.fa_debug_report.argtypes = [vp, ctypes.POINTER(i32)]
+            lib.fa_debug_report.restype = i32
             _lib = lib
     return _lib
 
@@ -350,3 +357,18 @@ def read_device_status(stream=None) -> int:
     if rc != FA_OK:
         raise RuntimeError(f"fa_read_device_status failed: {status_string(rc)}")
     return st.value
+
+
+def debug_build() -> bool:
+    """True when the loaded library is the debug build."""
+    return bool(load_library().fa_debug_build())
+
+
+def debug_report(stream=None) -> list[int]:
+    """Synchronise and return (then clear) the first failed device-side check of a
+    debug build: [check id, CTA, thread, a, b, 0, 0, failures]; all zeros if none."""
+    rec = (ctypes.c_int * 8)()
+    rc = load_library().fa_debug_report(_stream_handle(stream), rec)
+    if rc != FA_OK:
+        raise RuntimeError(f"fa_debug_report failed: {status_string(rc)}")
+    return list(rec)

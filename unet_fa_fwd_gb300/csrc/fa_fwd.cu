@@ -31,6 +31,8 @@
 // wait ran out of time.  Kernels in every translation unit receive its device
 // address in their parameters.
 __device__ int g_device_status = 0;
+// First failed device-side check of a debug build (see fa_debug_report).
+__device__ int g_debug_record[8] = {};
 
 namespace {
 
@@ -42,6 +44,7 @@ struct DeviceState {
   int device = 0;
   int sm_count = 0;
   int* status = nullptr;  // device address of g_device_status
+  int* debug_record = nullptr;  // device address of g_debug_record
 };
 
 std::mutex g_mutex;
@@ -86,6 +89,9 @@ int device_setup(int dev, DeviceState** out) {
     void* status = nullptr;
     if (cudaGetSymbolAddress(&status, g_device_status) != cudaSuccess || !status) return FA_ERR_CUDA;
     st.status = static_cast<int*>(status);
+    void* rec = nullptr;
+    if (cudaGetSymbolAddress(&rec, g_debug_record) != cudaSuccess || !rec) return FA_ERR_CUDA;
+    st.debug_record = static_cast<int*>(rec);
     if (!g_encode) {
       void* fn = nullptr;
       cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
@@ -220,6 +226,11 @@ int setup(const void* q, const void* k, const void* v, const float* mask, void* 
   prm->scale_log2 = (float)((double)scale * 1.4426950408889634);
   prm->timeout_ns = timeout_ns_from_env();
   prm->status = (*st)->status;
+  prm->debug_record = (*st)->debug_record;
+#ifdef FA_DEBUG
+  const char* plant = std::getenv("FA_DEBUG_PLANT");
+  prm->debug_plant = (plant && std::strcmp(plant, "store") == 0) ? 1 : 0;
+#endif
   prm->inject_stall = (inject && std::strcmp(inject, "stall") == 0) ? 1 : 0;
   return FA_OK;
 }
@@ -631,10 +642,42 @@ const char* fa_status_string(int status) {
     case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED";
     case FA_ERR_CUDA: return "FA_ERR_CUDA";
     case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT";
+    case FA_ERR_DEBUG_CHECK: return "FA_ERR_DEBUG_CHECK";
     default: return "FA_ERR_UNKNOWN";
   }
 }
 
-const char* fa_version(void) { return "unet_fa_fwd_gb300 0.1.0 sm_103a"; }
+int fa_debug_build(void) {
+#ifdef FA_DEBUG
+  return 1;
+#else
+  return 0;
+#endif
+}
+
+int fa_debug_report(void* stream, int* record) {
+  if (!record) return FA_ERR_INVALID_ARGUMENT;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int rec[8] = {};
+  if (cudaMemcpyFromSymbolAsync(rec, g_debug_record, sizeof(rec), 0, cudaMemcpyDeviceToHost, s) !=
+          cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return FA_ERR_CUDA;
+  const int zero[8] = {};
+  if (cudaMemcpyToSymbolAsync(g_debug_record, zero, sizeof(zero), 0, cudaMemcpyHostToDevice, s) !=
+          cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return FA_ERR_CUDA;
+  for (int i = 0; i < 8; ++i) record[i] = rec[i];
+  return FA_OK;
+}
+
+const char* fa_version(void) {
+#ifdef FA_DEBUG
+  return "unet_fa_fwd_gb300 0.2.0 sm_103a debug";
+#else
+  return "unet_fa_fwd_gb300 0.2.0 sm_103a";
+#endif
+}
 
 }  // extern "C"

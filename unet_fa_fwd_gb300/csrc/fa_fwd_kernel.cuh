@@ -36,7 +36,8 @@
 
 namespace fa {
 
-constexpr int kStatusTimeout = 4;  // == FA_ERR_TIMEOUT
+constexpr int kStatusTimeout = 4;     // == FA_ERR_TIMEOUT
+constexpr int kStatusDebugCheck = 5;  // == FA_ERR_DEBUG_CHECK
 constexpr uint32_t kSuspendNs = 20000;  // longest sleep inside one mbarrier poll
 
 
@@ -132,6 +133,8 @@ struct Params {
   int mask_heads;      // 1 (broadcast over heads) or H
   int qtiles;          // ceil(Nq/128)
   int* status;         // device status word: set to FA_ERR_TIMEOUT when a wait runs out
+  int* debug_record;   // debug builds: first failed device-side check (8 ints)
+  int debug_plant;     // debug builds, test hook: the O-store check uses bound Nq - 1
   __nv_bfloat16* out;  // [BH][Nq][D]
   float* lse;          // [BH][Nq]
   const float* mask;   // key padding [B][Nk] or nullptr
@@ -262,7 +265,52 @@ struct Barriers {
   uint32_t tmem_base;
   volatile int abort_flag;
   uint64_t kv_full[8], kv_empty[8];
+  int dbg_unit[3];  // debug builds: (unit, bh, q0) the producer loaded Q for
 };
+
+// Device-side checks of a debug build (-DFA_DEBUG): every global access and
+// the unit schedule are checked before use.  A failed check records the
+// first violation (check id, CTA, thread, two values; a count of failures),
+// sets FA_ERR_DEBUG_CHECK in the status word and the CTA's abort flag (so
+// every later wait returns and the CTA drains as after a timeout), and the
+// access is skipped.  Release builds compile every check to `true`.
+__device__ __forceinline__ bool fa_check(const Params& p, Barriers* bars, bool cond, int id,
+                                         long long a, long long b) {
+#ifdef FA_DEBUG
+  if (!cond) {
+    atomicCAS(p.status, 0, kStatusDebugCheck);
+    if (atomicCAS(&p.debug_record[0], 0, id) == 0) {
+      p.debug_record[1] = (int)blockIdx.x;
+      p.debug_record[2] = (int)threadIdx.x;
+      p.debug_record[3] = (int)a;
+      p.debug_record[4] = (int)b;
+    }
+    atomicAdd(&p.debug_record[7], 1);
+    bars->abort_flag = 1;
+  }
+  return cond;
+#else
+  (void)p; (void)bars; (void)id; (void)a; (void)b;
+  return cond || true;
+#endif
+}
+
+// Check ids.
+enum : int {
+  kCheckUnit = 1,       // decoded unit inside the problem (head, query pair, key blocks)
+  kCheckUnitSync = 2,   // the MMA warp's unit equals the one the producer loaded
+  kCheckMaskRow = 3,    // mask row inside the mask array
+  kCheckScale = 4,      // e4m3 block-scale index inside its array
+  kCheckStore = 5,      // O / LSE / partial store inside its array
+};
+
+// A decoded unit lies inside the problem.
+__device__ __forceinline__ bool unit_in_bounds(const Params& p, const Unit& un) {
+  return un.bh >= 0 && un.bh < p.BH && un.q0 >= 0 && un.q0 < p.Nq && (un.q0 & 127) == 0 &&
+         (un.nq == 1 || un.nq == 2) && un.q0 + 128 * (un.nq - 1) < p.Nq && un.tile0 >= 0 &&
+         un.ntiles >= 1 && un.tile0 + un.ntiles <= p.nkv && un.split >= 0 &&
+         un.split < p.num_splits;
+}
 
 // Bounded wait on an mbarrier phase.  Returns false if the CTA is aborting
 // (this wait ran out of time, or another one did).  Between polls the thread
@@ -496,6 +544,15 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
         const int ntiles = un.nq;
         ok = bounded_wait(ptx::smem_u32(&bars->q_empty), (uc & 1) ^ 1, bars, p.timeout_ns, p.status);
         if (!ok) break;
+        if (!fa_check(p, bars, unit_in_bounds(p, un), kCheckUnit, u, un.bh)) {
+          ok = false;  // drain this thread's copies in flight, as after a timeout
+          break;
+        }
+#ifdef FA_DEBUG
+        bars->dbg_unit[0] = u;
+        bars->dbg_unit[1] = bh;
+        bars->dbg_unit[2] = q0;
+#endif
         const uint32_t qbar = ptx::smem_u32(&bars->q_full);
         ptx::mbar_arrive_expect_tx(qbar, ntiles * C::QK_TILE_BYTES);
         for (int t = 0; t < ntiles; ++t)
@@ -643,6 +700,12 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
         const int nkv = un.ntiles;
         ok = bounded_wait_warp(ptx::smem_u32(&bars->q_full), uc & 1, bars, p.timeout_ns, p.status);
         if (!ok) break;
+#ifdef FA_DEBUG
+        ok = fa_check(p, bars, unit_in_bounds(p, un) && bars->dbg_unit[0] == u &&
+                                   bars->dbg_unit[1] == un.bh && bars->dbg_unit[2] == un.q0,
+                      kCheckUnitSync, u, bars->dbg_unit[0]);
+        if (!__all_sync(0xffffffffu, ok)) break;
+#endif
         ptx::tc_fence_after_sync();
         // Prologue: S for key block 0.
         uint32_t sK = 0, sV = 0;
@@ -726,6 +789,8 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
       const Unit un = decode_unit(p, u);
       const int bh = un.bh, q0 = un.q0;
       if (t == 1 && un.nq < 2) continue;
+      ok = __all_sync(0xffffffffu, fa_check(p, bars, unit_in_bounds(p, un), kCheckUnit, u, bh));
+      if (!ok) break;
       const int qrow = q0 + t * 128 + row;
       const int b_idx = (int)p.div_h.div((uint32_t)bh);  // batch entry of this head
       const float* mask_b = p.mask ? p.mask + (size_t)b_idx * p.Nk : nullptr;
@@ -741,7 +806,13 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
             (size_t)min(qrow, p.Nq - 1);
         mrow = static_cast<const uint8_t*>(p.full_mask) +
                fm_row * p.Nk * (p.full_mask_bool ? 1 : sizeof(float));
+        if (!fa_check(p, bars, fm_row < (size_t)(p.BH / p.H) * p.mask_heads * p.Nq, kCheckMaskRow,
+                      (long long)fm_row, bh))
+          mrow = p.full_mask;  // the first row: a valid address (results are discarded)
       }
+      if (mask_b != nullptr &&
+          !fa_check(p, bars, b_idx >= 0 && b_idx < p.BH / p.H, kCheckMaskRow, b_idx, bh))
+        mask_b = p.mask;
       // Keys of this row's segment (all keys when rows are not segmented).
       const int seg_lo = p.seg > 0 ? (qrow / p.seg) * p.seg : 0;
       const int seg_hi = p.seg > 0 ? seg_lo + p.seg : INT_MAX;
@@ -753,9 +824,13 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
         // log2-domain multiplier of raw S; with e4m3 Q and K it carries the
         // two block scales (positive, so its sign is the sign of `scale`).
         float sl2 = scale_log2;
-        if constexpr (F8)
-          sl2 *= __ldg(p.q_scale + (size_t)bh * p.qtiles + (tile_row0 >> 7)) *
-                 __ldg(p.k_scale + (size_t)bh * p.nkv + un.tile0 + j);
+        if constexpr (F8) {
+          const size_t qi = (size_t)bh * p.qtiles + (tile_row0 >> 7);
+          const size_t ki = (size_t)bh * p.nkv + un.tile0 + j;
+          if (fa_check(p, bars, qi < (size_t)p.BH * p.qtiles && ki < (size_t)p.BH * p.nkv,
+                       kCheckScale, (long long)qi, (long long)ki))
+            sl2 *= __ldg(p.q_scale + qi) * __ldg(p.k_scale + ki);
+        }
         // Fast path: full key block, no mask, non-negative scale — the scores
         // stay in registers and the row max is taken on raw scores, scaled
         // once.  Otherwise (general path) scores are materialised in the log2
@@ -980,22 +1055,31 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
               w[k] = v;
             }
             const int orow = warp_row0 + src;
+#ifdef FA_DEBUG
+            const int nq_bound = p.debug_plant ? p.Nq - 1 : p.Nq;
+            if (orow < p.Nq && fa_check(p, bars, orow < nq_bound && bh < p.BH, kCheckStore,
+                                        (long long)bh * p.Nq + orow, cb))
+#else
             if (orow < p.Nq)
+#endif
               *reinterpret_cast<uint4*>(p.out + ((size_t)bh * p.Nq + orow) * D + cb + piece * 8) =
                   make_uint4(w[0], w[1], w[2], w[3]);
           }
         }
-        if (valid_row) p.lse[(size_t)bh * p.Nq + qrow] = row_lse;
+        if (valid_row && fa_check(p, bars, bh < p.BH, kCheckStore, (long long)bh * p.Nq + qrow, -1))
+          p.lse[(size_t)bh * p.Nq + qrow] = row_lse;
       } else {
         // Split mode: this key range's normalised O (fp32) and its LSE, merged
         // by fa_merge_kernel.
         const size_t prow = ((size_t)un.split * p.BH + bh) * p.Nq + (valid_row ? qrow : 0);
         float* orow = p.part_o + prow * D;
+        const bool prow_ok = fa_check(p, bars, prow < (size_t)p.num_splits * p.BH * p.Nq,
+                                      kCheckStore, (long long)prow, -2);
 #pragma unroll
         for (int cb = 0; cb < D; cb += 32) {
           uint32_t r[32];
           ptx::tmem_ld32x32b_x32(tO + cb, r);
-          if (valid_row) {
+          if (valid_row && prow_ok) {
             float4* dst = reinterpret_cast<float4*>(orow + cb);
 #pragma unroll
             for (int v4 = 0; v4 < 8; ++v4)
@@ -1005,7 +1089,7 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
                                     __uint_as_float(r[4 * v4 + 3]) * inv_l);
           }
         }
-        if (valid_row) p.part_lse[prow] = row_lse;
+        if (valid_row && prow_ok) p.part_lse[prow] = row_lse;
       }
     }
     ptx::tc_fence_before_sync();
