@@ -25,6 +25,13 @@
 
 #include <stddef.h>
 
+/* The library exports these functions only; everything else is hidden. */
+#if defined(__GNUC__)
+#define FA_API __attribute__((visibility("default")))
+#else
+#define FA_API
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -69,7 +76,7 @@ typedef enum {
  * of time on an internal wait records FA_ERR_TIMEOUT in the device status
  * word (see fa_read_device_status) and exits without hanging.
  */
-int fa_fwd(const void* q, const void* k, const void* v, const float* mask, void* out, float* lse,
+FA_API int fa_fwd(const void* q, const void* k, const void* v, const float* mask, void* out, float* lse,
            int B, int H, int Nq, int Nk, int D, float scale, void* stream);
 
 /* Kinds of mask fa_fwd_ex accepts. */
@@ -108,7 +115,7 @@ typedef struct fa_mask {
  * FA_ERR_INVALID_ARGUMENT for an unknown kind, NULL data, heads not 1 or H,
  * or a misaligned or overlapping mask.
  */
-int fa_fwd_ex(const void* q, const void* k, const void* v, const fa_mask* mask, int causal,
+FA_API int fa_fwd_ex(const void* q, const void* k, const void* v, const fa_mask* mask, int causal,
               void* out, float* lse, int B, int H, int Nq, int Nk, int D, float scale,
               void* stream);
 
@@ -136,12 +143,12 @@ int fa_fwd_ex(const void* q, const void* k, const void* v, const fa_mask* mask, 
  * quantise Q, attention).  Errors as fa_fwd, plus FA_ERR_INVALID_ARGUMENT for
  * a missing, misaligned, small or overlapping workspace.
  */
-int fa_fwd_fp8(const void* q, const void* k, const void* v, const float* mask, void* out,
+FA_API int fa_fwd_fp8(const void* q, const void* k, const void* v, const float* mask, void* out,
                float* lse, int B, int H, int Nq, int Nk, int D, float scale, void* workspace,
                size_t workspace_bytes, void* stream);
 
 /* Workspace bytes fa_fwd_fp8 needs (0 for invalid sizes). */
-size_t fa_fp8_workspace_bytes(int B, int H, int Nq, int Nk, int D);
+FA_API size_t fa_fp8_workspace_bytes(int B, int H, int Nq, int Nk, int D);
 
 /*
  * fa_fwd_split — the same forward with the key axis cut into `num_splits`
@@ -169,19 +176,19 @@ size_t fa_fp8_workspace_bytes(int B, int H, int Nq, int Nk, int D);
  * missing, misaligned, too small or overlapping workspace.  Two kernels are
  * enqueued on `stream` (the split forward, then the merge).
  */
-int fa_fwd_split(const void* q, const void* k, const void* v, const float* mask, void* out,
+FA_API int fa_fwd_split(const void* q, const void* k, const void* v, const float* mask, void* out,
                  float* lse, int B, int H, int Nq, int Nk, int D, float scale, int num_splits,
                  void* workspace, size_t workspace_bytes, void* stream);
 
 /* Workspace bytes fa_fwd_split needs for these sizes (0 for invalid sizes). */
-size_t fa_split_workspace_bytes(int B, int H, int Nq, int D, int num_splits);
+FA_API size_t fa_split_workspace_bytes(int B, int H, int Nq, int D, int num_splits);
 
 /*
  * A key-range count for fa_fwd_split on a GPU with `num_sms` SMs: 1 when the
  * unsplit work units already cover every SM, else enough ranges to do so,
  * each range at least four 128-key blocks long.  Pure arithmetic; no CUDA call.
  */
-int fa_split_count(int B, int H, int Nq, int Nk, int num_sms);
+FA_API int fa_split_count(int B, int H, int Nq, int Nk, int num_sms);
 
 /*
  * fa_fwd_window — window / shifted-window attention on an img_h x img_w token
@@ -205,12 +212,12 @@ int fa_split_count(int B, int H, int Nq, int Nk, int num_sms);
  * Errors as fa_fwd, plus FA_ERR_INVALID_ARGUMENT for windows that do not tile
  * the grid or a missing, misaligned, small or overlapping workspace.
  */
-int fa_fwd_window(const void* q, const void* k, const void* v, void* out, float* lse, int B, int H,
+FA_API int fa_fwd_window(const void* q, const void* k, const void* v, void* out, float* lse, int B, int H,
                   int img_h, int img_w, int D, int win_h, int win_w, int shift_h, int shift_w,
                   float scale, void* workspace, size_t workspace_bytes, void* stream);
 
 /* Workspace bytes fa_fwd_window needs (0 for invalid sizes). */
-size_t fa_window_workspace_bytes(int B, int H, int img_h, int img_w, int D);
+FA_API size_t fa_window_workspace_bytes(int B, int H, int img_h, int img_w, int D);
 
 /* Bytes of the fixed device scratch that fa_fwd_split_noalloc uses. */
 #define FA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
@@ -235,7 +242,7 @@ size_t fa_window_workspace_bytes(int B, int H, int img_h, int img_w, int D);
  * call's contents: calls that overlap on the GPU (other streams, or before the
  * previous call finished) race on it and must be serialised by the caller.
  */
-int fa_fwd_split_noalloc(const void* q, const void* k, const void* v, const float* mask, void* out,
+FA_API int fa_fwd_split_noalloc(const void* q, const void* k, const void* v, const float* mask, void* out,
                          float* lse, int B, int H, int Nq, int Nk, int D, float scale,
                          int num_splits, void* stream);
 
@@ -245,7 +252,7 @@ int fa_fwd_split_noalloc(const void* q, const void* k, const void* v, const floa
  * Synchronises `stream` first.  Writes FA_OK or FA_ERR_TIMEOUT to *status.
  * Returns FA_OK, FA_ERR_INVALID_ARGUMENT (status NULL) or FA_ERR_CUDA.
  */
-int fa_read_device_status(void* stream, int* status);
+FA_API int fa_read_device_status(void* stream, int* status);
 
 /*
  * fa_measure_ex2_rate — throughput of the exponential the forward takes once
@@ -261,7 +268,7 @@ int fa_read_device_status(void* stream, int* status);
  * FA_ERR_INVALID_ARGUMENT (NULL output), FA_ERR_UNSUPPORTED (more than 1024
  * SMs) or FA_ERR_CUDA.
  */
-int fa_measure_ex2_rate(void* stream, double* ex2_per_clock_per_sm);
+FA_API int fa_measure_ex2_rate(void* stream, double* ex2_per_clock_per_sm);
 
 /*
  * Debug build (libfa_fwd_debug.so, compiled with FA_DEBUG; no counterpart on
@@ -280,14 +287,14 @@ int fa_measure_ex2_rate(void* stream, double* ex2_per_clock_per_sm);
  *   The release build writes zeros.  Returns FA_OK, FA_ERR_INVALID_ARGUMENT
  *   (record NULL) or FA_ERR_CUDA.
  */
-int fa_debug_build(void);
-int fa_debug_report(void* stream, int* record);
+FA_API int fa_debug_build(void);
+FA_API int fa_debug_report(void* stream, int* record);
 
 /* Human-readable name of a status code (static storage; never NULL). */
-const char* fa_status_string(int status);
+FA_API const char* fa_status_string(int status);
 
 /* Library version string, e.g. "unet_fa_fwd_gb300 0.1.0 sm_103a" (static storage). */
-const char* fa_version(void);
+FA_API const char* fa_version(void);
 
 #ifdef __cplusplus
 }

@@ -44,7 +44,11 @@ def _obj(unit: str, debug: bool) -> str:
 
 
 def compile_cmd(unit: str, debug: bool = False, extra: list[str] | None = None) -> list[str]:
-    return [_nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE,
+    # Host symbols are hidden except the C ABI (FA_API in fa.h), so two builds of
+    # the library (release and debug) can share a process without interposing
+    # each other's template instantiations.
+    return [_nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
+            "-Xcompiler", "-fvisibility=hidden", "-I", INCLUDE,
             "-I", CSRC, *(["-DFA_DEBUG"] if debug else []), "-c", "-o", _obj(unit, debug),
             os.path.join(CSRC, unit), *(extra or [])]
 

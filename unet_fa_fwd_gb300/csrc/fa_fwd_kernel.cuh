@@ -166,13 +166,18 @@ struct Unit {
 __device__ __forceinline__ Unit decode_unit(const Params& p, int u) {
   Unit r;
   const uint32_t upb = (uint32_t)p.units_per_bh;
+  // Pair index -> (head, first query row), head-major.
+  auto locate = [&](uint32_t pair, int& bh, int& q0) {
+    const uint32_t k = p.div_upb.div(pair);
+    bh = (int)k;
+    q0 = (int)(pair - k * upb) * 256;
+  };
   if (u >= p.tail_start) {
     const uint32_t v = (uint32_t)(u - p.tail_start);
     const uint32_t pair = (uint32_t)p.tail_start + (v >> 1);  // unsplit launch: unit == pair index
-    const uint32_t bh = p.div_upb.div(pair);
+    locate(pair, r.bh, r.q0);
     r.split = 0;
-    r.bh = (int)bh;
-    r.q0 = (int)(pair - bh * upb) * 256 + (int)(v & 1) * 128;
+    r.q0 += (int)(v & 1) * 128;
     r.nq = 1;
   } else if (p.causal) {
     // Causal (one key range): a pair's work grows with its query position, so
@@ -191,9 +196,7 @@ __device__ __forceinline__ Unit decode_unit(const Params& p, int u) {
       rest = p.div_splits.div((uint32_t)u);
       r.split = u - (int)rest * p.num_splits;
     }
-    const uint32_t bh = p.div_upb.div(rest);
-    r.bh = (int)bh;
-    r.q0 = (int)(rest - bh * upb) * 256;
+    locate(rest, r.bh, r.q0);
     r.nq = (r.q0 + 128 < p.Nq) ? 2 : 1;
   }
   if (p.num_splits == 1) {
