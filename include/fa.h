@@ -139,8 +139,8 @@ FA_API int fa_fwd_ex(const void* q, const void* k, const void* v, const fa_mask*
  *              fa_fp8_workspace_bytes(B, H, Nq, Nk, D) bytes, owned by the caller
  *              and not shared with a concurrent call.
  *
- * Five kernels are enqueued on `stream` (column sums, mean, quantise K,
- * quantise Q, attention).  Errors as fa_fwd, plus FA_ERR_INVALID_ARGUMENT for
+ * Four kernels are enqueued on `stream` (column sums of K, their means, the
+ * quantisation of K and Q, attention).  Errors as fa_fwd, plus FA_ERR_INVALID_ARGUMENT for
  * a missing, misaligned, small or overlapping workspace.
  */
 FA_API int fa_fwd_fp8(const void* q, const void* k, const void* v, const float* mask, void* out,

@@ -285,24 +285,22 @@ F8Layout f8_layout(int B, int H, int Nq, int Nk, int D) {
 template <int D>
 void launch_quant(const void* q, const void* k, char* ws, const F8Layout& L, int BH, int Nq, int Nk,
                   float scale, cudaStream_t s) {
+  const int kt = (Nk + 127) / 128, qt = (Nq + 127) / 128;
+  fa::log_launch("fa_k_colsum_kernel<D=%d> grid %d x %d; fa_k_mean_kernel grid %d; "
+                 "fa_quant_kernel<D=%d> grid %d (%d K blocks + %d Q blocks; 256 threads each)",
+                 D, BH, kF8ColsumSplits, (BH * D + 255) / 256, D, BH * (kt + qt), BH * kt, BH * qt);
   fa::fa_k_colsum_kernel<D><<<dim3(BH, kF8ColsumSplits), 256, 0, s>>>(
       static_cast<const __nv_bfloat16*>(k), reinterpret_cast<float*>(ws + L.partial), Nk,
       kF8ColsumSplits);
   fa::fa_k_mean_kernel<<<(BH * D + 255) / 256, 256, 0, s>>>(
       reinterpret_cast<const float*>(ws + L.partial), reinterpret_cast<float*>(ws + L.mean), BH, D,
       kF8ColsumSplits, Nk);
-  const int kt = (Nk + 127) / 128, qt = (Nq + 127) / 128;
-  fa::log_launch("fa_k_colsum_kernel<D=%d> grid %d x %d; fa_k_mean_kernel grid %d; "
-             "fa_quant_rows_kernel<K> grid %d; fa_quant_rows_kernel<Q> grid %d (256 threads each)",
-             D, BH, kF8ColsumSplits, (BH * D + 255) / 256, BH * kt, BH * qt);
-  fa::fa_quant_rows_kernel<D, true><<<BH * kt, 256, 0, s>>>(
-      static_cast<const __nv_bfloat16*>(k), reinterpret_cast<const float*>(ws + L.mean),
-      reinterpret_cast<uint8_t*>(ws + L.k8), reinterpret_cast<float*>(ws + L.k_scale), nullptr, Nk,
-      kt, scale);
-  fa::fa_quant_rows_kernel<D, false><<<BH * qt, 256, 0, s>>>(
-      static_cast<const __nv_bfloat16*>(q), reinterpret_cast<const float*>(ws + L.mean),
-      reinterpret_cast<uint8_t*>(ws + L.q8), reinterpret_cast<float*>(ws + L.q_scale),
-      reinterpret_cast<float*>(ws + L.corr), Nq, qt, scale);
+  fa::fa_quant_kernel<D><<<BH * (kt + qt), 256, 0, s>>>(
+      static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(q),
+      reinterpret_cast<const float*>(ws + L.mean),
+      reinterpret_cast<uint8_t*>(ws + L.k8), reinterpret_cast<uint8_t*>(ws + L.q8),
+      reinterpret_cast<float*>(ws + L.k_scale), reinterpret_cast<float*>(ws + L.q_scale),
+      reinterpret_cast<float*>(ws + L.corr), BH, Nk, Nq, kt, qt, scale);
 }
 
 // Key ranges actually used for a requested count: at most one per key block,

@@ -10,8 +10,9 @@
 //   q_scale[b] = max |Q|  over 128-row block b / 448, Q8 = e4m3(Q / q_scale)
 //   lse_corr_i = scale * (q_i . mean_k)                added back to LSE_i
 //
-// 448 is the largest finite e4m3 value.  All kernels are bound by HBM
-// bandwidth (each reads its bf16 input once and writes one byte per element).
+// 448 is the largest finite e4m3 value.  Three launches: the column sums of K,
+// their means, then the quantisation of K and Q (HBM bound: each input read
+// once, one byte written per element).
 #pragma once
 
 #include <cuda_bf16.h>
@@ -40,6 +41,7 @@ __global__ void __launch_bounds__(256) fa_k_colsum_kernel(const __nv_bfloat16* _
 #pragma unroll
   for (int e = 0; e < 8; ++e) acc[e] = 0.f;
   const uint4* base = reinterpret_cast<const uint4*>(k + (size_t)bh * Nk * D) + part;
+#pragma unroll 4
   for (int t = t0 + r; t < t1; t += RL) {
     const uint4 u = __ldg(base + (size_t)t * PARTS);
     const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&u);
@@ -62,6 +64,7 @@ __global__ void __launch_bounds__(256) fa_k_colsum_kernel(const __nv_bfloat16* _
   }
 }
 
+// Channel means of K: mean[bh][c] = (sum of the nsplit partial sums) / Nk.
 __global__ void fa_k_mean_kernel(const float* __restrict__ partial, float* __restrict__ mean,
                                  int BH, int D, int nsplit, int Nk) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
@@ -72,53 +75,71 @@ __global__ void fa_k_mean_kernel(const float* __restrict__ partial, float* __res
   mean[i] = sum / (float)Nk;
 }
 
-// One CTA of 256 threads per (bh, 128-row block).  The block's rows are read
-// as 16-byte chunks (8 elements), chunk i by thread i mod 256, so a warp's
-// loads and its 8-byte e4m3 stores cover whole rows contiguously.  The block
-// max goes through shared memory; the Q row dot with mean(K) (for lse_corr) is
-// reduced across the D/8 lanes holding one row.
-// IS_K: subtract the channel mean first.  Q: also write scale * (q_i . mean_k).
-template <int D, bool IS_K>
-__global__ void __launch_bounds__(256) fa_quant_rows_kernel(
-    const __nv_bfloat16* __restrict__ x, const float* __restrict__ mean_k, uint8_t* __restrict__ x8,
-    float* __restrict__ block_scale, float* __restrict__ lse_corr, int N, int nblk, float scale) {
+// Quantisation of K and Q in one launch: CTAs [0, BH*kt) take 128-key blocks
+// of K, the rest 128-row blocks of Q.  Each CTA reads its block as 16-byte
+// chunks (8 elements), chunk i by thread i mod 256, so a warp's
+// loads and its 8-byte e4m3 stores cover whole rows contiguously.  A thread
+// always holds the same 8 channels (256 is a multiple of the chunks per row),
+// so it keeps their means in registers.  K: smoothed by the mean
+// first.  Q: also writes lse_corr = scale * (q_i . mean_k), reduced across the
+// D/8 lanes holding a row.
+template <int D>
+__global__ void __launch_bounds__(256, 2) fa_quant_kernel(
+    const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ q,
+    const float* __restrict__ mean_k, uint8_t* __restrict__ k8,
+    uint8_t* __restrict__ q8, float* __restrict__ k_scale, float* __restrict__ q_scale,
+    float* __restrict__ lse_corr, int BH, int Nk, int Nq, int kt, int qt, float scale) {
   constexpr int PARTS = D / 8;                 // chunks per row (4, 8 or 16)
   constexpr int PER = 128 * PARTS / 256;       // chunks per thread (2, 4 or 8)
-  const int bh = blockIdx.x / nblk, blk = blockIdx.x % nblk;
+  const bool is_k = (int)blockIdx.x < BH * kt;
+  const int cta = is_k ? (int)blockIdx.x : (int)blockIdx.x - BH * kt;
+  const int nblk = is_k ? kt : qt;
+  const int N = is_k ? Nk : Nq;
+  const int bh = cta / nblk, blk = cta % nblk;
   const int tid = threadIdx.x;
-  __shared__ float smean[D];
+  const int part = tid % PARTS;                // this thread's 8 channels: part*8 .. +7
+
   __shared__ float wmax[8];
-  for (int c = tid; c < D; c += 256) smean[c] = mean_k[(size_t)bh * D + c];
-  __syncthreads();
+  // the 8 channel means of this thread's chunk column
+  float mean[8];
+  {
+    const float4* m4 = reinterpret_cast<const float4*>(mean_k + (size_t)bh * D + part * 8);
+    const float4 a = __ldg(m4), b = __ldg(m4 + 1);
+    mean[0] = a.x; mean[1] = a.y; mean[2] = a.z; mean[3] = a.w;
+    mean[4] = b.x; mean[5] = b.y; mean[6] = b.z; mean[7] = b.w;
+  }
 
   const size_t row0 = (size_t)bh * N + (size_t)blk * 128;
-  const uint4* src = reinterpret_cast<const uint4*>(x + row0 * D);
+  const uint4* src = reinterpret_cast<const uint4*>((is_k ? k : q) + row0 * D);
+  uint4 raw[PER];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    const int r = (i * 256 + tid) / PARTS;
+    raw[i] = blk * 128 + r < N ? __ldg(src + i * 256 + tid) : make_uint4(0u, 0u, 0u, 0u);
+  }
+  // fp32 values of the chunks (smoothed for K; rows past N are zero)
   float val[PER][8];
   float amax = 0.f;
 #pragma unroll
   for (int i = 0; i < PER; ++i) {
-    const int chunk = i * 256 + tid;
-    const int r = chunk / PARTS, part = chunk % PARTS;
-    const bool valid = blk * 128 + r < N;
-    uint4 u = make_uint4(0u, 0u, 0u, 0u);
-    if (valid) u = __ldg(src + chunk);
-    const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&u);
+    const int r = (i * 256 + tid) / PARTS;
+    const bool smooth = is_k && blk * 128 + r < N;
+    const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&raw[i]);
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const float2 f = __bfloat1622float2(h2[e]);
-      const int c = part * 8 + 2 * e;
-      val[i][2 * e] = (IS_K && valid) ? f.x - smean[c] : f.x;
-      val[i][2 * e + 1] = (IS_K && valid) ? f.y - smean[c + 1] : f.y;
+      val[i][2 * e] = smooth ? f.x - mean[2 * e] : f.x;
+      val[i][2 * e + 1] = smooth ? f.y - mean[2 * e + 1] : f.y;
     }
 #pragma unroll
     for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(val[i][e]));
-    if (!IS_K) {
+    if (!is_k) {
       float dot = 0.f;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) dot = fmaf(val[i][e], smean[part * 8 + e], dot);
+      for (int e = 0; e < 8; ++e) dot = fmaf(val[i][e], mean[e], dot);
 #pragma unroll
       for (int o = PARTS / 2; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-      if (part == 0 && valid) lse_corr[row0 + r] = scale * dot;
+      if (part == 0 && blk * 128 + r < N) lse_corr[row0 + r] = scale * dot;
     }
   }
 #pragma unroll
@@ -130,8 +151,8 @@ __global__ void __launch_bounds__(256) fa_quant_rows_kernel(
   for (int w = 1; w < 8; ++w) amax = fmaxf(amax, wmax[w]);
   const float s = amax > 0.f ? amax / kE4M3Max : 1.f;
   const float inv = 1.f / s;
-  if (tid == 0) block_scale[(size_t)bh * nblk + blk] = s;
-  uint2* dst = reinterpret_cast<uint2*>(x8 + row0 * D);
+  if (tid == 0) (is_k ? k_scale : q_scale)[(size_t)bh * nblk + blk] = s;
+  uint2* dst = reinterpret_cast<uint2*>((is_k ? k8 : q8) + row0 * D);
 #pragma unroll
   for (int i = 0; i < PER; ++i) {
     const int chunk = i * 256 + tid;
@@ -143,9 +164,9 @@ __global__ void __launch_bounds__(256) fa_quant_rows_kernel(
       uint32_t word = 0;
 #pragma unroll
       for (int b = 0; b < 4; ++b) {
-        const __nv_fp8_storage_t q8 =
+        const __nv_fp8_storage_t v8 =
             __nv_cvt_float_to_fp8(val[i][4 * h + b] * inv, __NV_SATFINITE, __NV_E4M3);
-        word |= (uint32_t)q8 << (8 * b);
+        word |= (uint32_t)v8 << (8 * b);
       }
       w[h] = word;
     }
