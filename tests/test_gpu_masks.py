@@ -157,3 +157,32 @@ def test_mask_base_not_vector_aligned(kind):
     out, lse = _run(inp, full_mask=m)
     o_ref, l_ref = _oracle(inp, full_mask=ref_mask)
     compare(out, lse, o_ref, l_ref, label=f"{kind} mask, unaligned base")
+
+
+@pytest.mark.parametrize("D", [32, 64, 128])
+@pytest.mark.parametrize("kind", ["additive", "bool"])
+@pytest.mark.parametrize("per_head", [False, True])
+def test_staged_mask_many_units(D, kind, per_head):
+    """Mask rows 16-byte aligned (Nk 1040): an fp32 mask is copied tile by
+    tile into shared memory (a byte mask takes 16-byte loads).  More units than
+    SMs, so a CTA runs several units (the mask pieces are counted across them);
+    Nq 600 ends on a partial tile."""
+    G = torch.cuda.get_device_properties(0).multi_processor_count
+    B, H, Nq, Nk = 1, G // 2 + 7, 600, 1040
+    inp = _inputs(D, B, H, Nq, Nk)
+    g = torch.Generator(device="cuda").manual_seed(11)
+    mh = H if per_head else 1
+    if kind == "additive":
+        m = torch.randn(B, mh, Nq, Nk, generator=g, device="cuda") * 2
+        m[0, :, 5, :] = float("-inf")                 # a fully masked row
+        m[0, :, 300:420, 128:300] = float("-inf")     # whole and partial masked blocks
+        ref = m
+    else:
+        m = torch.rand(B, mh, Nq, Nk, generator=g, device="cuda") > 0.4
+        m[..., 0] = True
+        m[0, :, 300:420, 128:300] = False
+        ref = torch.where(m, 0.0, float("-inf")).float()
+    rows = workloads.sample_rows(Nq, B * H, 96, seed=D)
+    out, lse = _run(inp, full_mask=m.contiguous())
+    o_ref, l_ref = _oracle(inp, full_mask=ref, rows=rows)
+    compare(out, lse, o_ref, l_ref, rows=rows, label=f"staged {kind} D{D} heads {mh}")

@@ -16,7 +16,7 @@ constexpr int kLaunchMaxDevices = 64;
 
 template <int D, bool F8, int MK>
 int launch_one(const Params& prm, int device, int sm_count, cudaStream_t stream) {
-  using C = Cfg<D, F8>;
+  using C = Cfg<D, F8, MK>;
   static std::mutex mu;
   static bool ready[kLaunchMaxDevices] = {};
   if (device < 0 || device >= kLaunchMaxDevices) return FA_ERR_CUDA;
@@ -37,7 +37,8 @@ int launch_one(const Params& prm, int device, int sm_count, cudaStream_t stream)
     }
   }
   const int grid = prm.num_units < sm_count ? prm.num_units : sm_count;
-  static const char* kMaskNames[] = {"none", "fp32x4", "fp32", "u8x16", "u8"};
+  static const char* kMaskNames[] = {"none", "fp32x4", "fp32", "u8x16", "u8",
+                                      "fp32 staged"};
   log_launch("fa_fwd_kernel<D=%d,%s,mask %s> tile %dx%d grid %d x %d threads smem %d B tmem %d cols "
              "stages %d units %d (single-tile from %d) key ranges %d BH %d Nq %d Nk %d "
              "mask %s causal %d seg %d",
@@ -68,6 +69,7 @@ int launch_attention(const Params& prm, bool f8, int device, int sm_count, cudaS
     case kMaskF32Scalar: return launch_one<D, false, kMaskF32Scalar>(prm, device, sm_count, stream);
     case kMaskU8Vec: return launch_one<D, false, kMaskU8Vec>(prm, device, sm_count, stream);
     case kMaskU8Scalar: return launch_one<D, false, kMaskU8Scalar>(prm, device, sm_count, stream);
+    case kMaskF32Staged: return launch_one<D, false, kMaskF32Staged>(prm, device, sm_count, stream);
     default: return FA_ERR_UNSUPPORTED;
   }
 }

@@ -47,6 +47,12 @@ struct DeviceState {
   int* debug_record = nullptr;  // device address of g_debug_record
 };
 
+// Build option: 0 reads fp32 per-(query, key) masks with plain loads too (the
+// staged TMA path is then never selected).
+#ifndef FA_STAGED_MASK
+#define FA_STAGED_MASK 1
+#endif
+
 std::mutex g_mutex;
 DeviceState g_devices[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -120,6 +126,23 @@ int encode_map(CUtensorMap* map, const void* base, int BH, int N, int D) {
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
                         strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         sw_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
+// 4-D tensor map over a per-(query, key) fp32 mask [B][heads][Nq][Nk] (Nk a
+// multiple of 4).  Box = 128 query rows x 32 keys (128 bytes), 128-byte
+// swizzle.  Coordinates past Nq or Nk read zeros (those rows and keys are
+// never used).
+int encode_mask_map(CUtensorMap* map, const void* base, int B, int heads, int Nq, int Nk) {
+  cuuint64_t dims[4] = {(cuuint64_t)Nk, (cuuint64_t)Nq, (cuuint64_t)heads, (cuuint64_t)B};
+  cuuint64_t strides[3] = {(cuuint64_t)Nk * 4, (cuuint64_t)Nq * Nk * 4,
+                           (cuuint64_t)heads * Nq * Nk * 4};
+  cuuint32_t box[4] = {32u, 128u, 1u, 1u};
+  cuuint32_t estride[4] = {1u, 1u, 1u, 1u};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                        4, const_cast<void*>(base), dims, strides, box, estride,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
@@ -364,12 +387,23 @@ int fa_fwd_ex(const void* q, const void* k, const void* v, const fa_mask* mask, 
     prm.full_mask = mask->data;
     prm.full_mask_bool = kind == FA_MASK_BOOL;
     prm.mask_heads = mask->heads;
-    // 16-byte loads when every mask row starts 16-byte aligned.
-    const bool base16 = aligned16(mask->data);
-    if (kind == FA_MASK_BOOL)
-      prm.mask_kind = (base16 && Nk % 16 == 0) ? fa::kMaskU8Vec : fa::kMaskU8Scalar;
-    else
-      prm.mask_kind = (base16 && Nk % 4 == 0) ? fa::kMaskF32Vec : fa::kMaskF32Scalar;
+    // When every mask row starts 16-byte aligned (Nk * element size a
+    // multiple of 16 and an aligned base), an fp32 mask is staged (copied by
+    // TMA into shared memory tile by tile) and a byte mask is read with
+    // 16-byte loads; otherwise each lane reads its row element by element.
+    // (A byte mask is a quarter of the traffic: its plain loads measured
+    // faster than staging it, which costs K/V ring depth.)
+    const bool bytes = kind == FA_MASK_BOOL;
+    const bool rows16 = aligned16(mask->data) && Nk % (bytes ? 16 : 4) == 0;
+    if (bytes) {
+      prm.mask_kind = rows16 ? fa::kMaskU8Vec : fa::kMaskU8Scalar;
+    } else if (rows16 && FA_STAGED_MASK) {
+      if (encode_mask_map(&prm.tm_mask, mask->data, B, mask->heads, Nq, Nk) != FA_OK)
+        return FA_ERR_CUDA;
+      prm.mask_kind = fa::kMaskF32Staged;
+    } else {
+      prm.mask_kind = rows16 ? fa::kMaskF32Vec : fa::kMaskF32Scalar;
+    }
   }
   prm.causal = causal ? 1 : 0;
   return launch_fwd(prm, *st, D, reinterpret_cast<cudaStream_t>(stream));

@@ -41,9 +41,31 @@ constexpr int kStatusDebugCheck = 5;  // == FA_ERR_DEBUG_CHECK
 constexpr uint32_t kSuspendNs = 20000;  // longest sleep inside one mbarrier poll
 
 
+// How the general softmax path reads additive mask values, one kind per
+// launch (chosen on the host from the mask, Nk and the alignment): none (only
+// the key-range checks), fp32 or uint8 values of one row read 16 bytes per
+// load (row starts 16-byte aligned), or one element per load.  The key-padding
+// mask [B][Nk] is a row shared by every query row of a batch entry.  The
+// staged kind (a per-(query, key) fp32 mask whose rows are 16-byte multiples)
+// is copied by TMA into shared memory in 16 KB pieces of 128 rows x 32 keys by
+// a producer warp, ahead of the softmax.
+enum : int {
+  kMaskNone = 0,
+  kMaskF32Vec = 1,
+  kMaskF32Scalar = 2,
+  kMaskU8Vec = 3,
+  kMaskU8Scalar = 4,
+  kMaskF32Staged = 5,
+};
+// Staged mask ring: slots of 16 KB (128 rows x 128 bytes) and the full
+// barriers that signal them (two per slot; the reason is given in Cfg).
+constexpr int kMaskSlots = 4;
+constexpr int kMaskFullBars = 2 * kMaskSlots;
+
 // F8: Q and K are e4m3 (one byte) with per-128-row block scales and
-// S = Q K^T runs as kind::f8f6f4 MMAs; V and P stay bf16.
-template <int D, bool F8 = false>
+// S = Q K^T runs as kind::f8f6f4 MMAs; V and P stay bf16.  MK: mask kind
+// (the staged kind takes shared memory from the K/V ring).
+template <int D, bool F8 = false, int MK = kMaskNone>
 struct Cfg {
   static_assert(D == 32 || D == 64 || D == 128, "head dim");
   static constexpr int BM = 128;                       // query rows per tile
@@ -74,12 +96,31 @@ struct Cfg {
 #ifndef FA_STAGES_D128
 #define FA_STAGES_D128 5
 #endif
+  // Staged mask pieces: 16 KB each (128 rows x 32 fp32 keys, 128-byte
+  // swizzle), a ring of MASK_SLOTS, MASK_PIECES per 128-key block per query
+  // tile.
+  static constexpr bool STAGED_MASK = MK == kMaskF32Staged;
+  static constexpr int MASK_SLOTS = kMaskSlots;
+  // Piece i lands on full barrier i mod MASK_FULL_BARS.  The two warpgroups
+  // take pieces alternately (a block's pieces for tile 0, then for tile 1),
+  // so a warp may wait for a piece up to 2 * MASK_PIECES - 1 pieces ahead of
+  // the oldest one not yet consumed; with one barrier per slot that wait could
+  // be two phases ahead of the barrier and its parity test would pass at
+  // once.  Two barriers per slot keep every wait within one phase.
+  static constexpr int MASK_FULL_BARS = kMaskFullBars;
+  static constexpr int MASK_PIECE_BYTES = 128 * 128;
+  static constexpr int MASK_PIECE_KEYS = 32;
+  static constexpr int MASK_PIECES = 128 / MASK_PIECE_KEYS;
   // K/V ring depth: as deep as shared memory allows (227 KB per CTA).
-  static constexpr int STAGES = (D == 128) ? (F8 ? 6 : FA_STAGES_D128) : (D == 64 ? 6 : 8);
+  static constexpr int STAGES = STAGED_MASK ? ((D == 128) ? 3 : (D == 64 ? 4 : 8))
+                                            : ((D == 128) ? (F8 ? 6 : FA_STAGES_D128)
+                                                          : (D == 64 ? 6 : 8));
   static constexpr int SMEM_Q = 2 * QK_TILE_BYTES;
+  static constexpr int SMEM_MASK = STAGED_MASK ? MASK_SLOTS * MASK_PIECE_BYTES : 0;
   static constexpr int SMEM_RING = STAGES * TILE_BYTES;
   static constexpr int SMEM_BAR = 1024;
-  static constexpr int SMEM_USED = 1024 /*align slack*/ + SMEM_Q + SMEM_RING + SMEM_BAR;
+  static constexpr int SMEM_USED =
+      1024 /*align slack*/ + SMEM_Q + SMEM_MASK + SMEM_RING + SMEM_BAR;
   // 512 TMEM columns per CTA => one CTA per SM; pad shared memory so that a
   // second CTA never lands on the SM and blocks in tcgen05.alloc.
   static constexpr int SMEM_BYTES = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;
@@ -148,6 +189,7 @@ struct Params {
   CUtensorMap tm_q;  // [BH][Nq][D] bf16 (e4m3 for the F8 kernel)
   CUtensorMap tm_k;  // [BH][Nk][D]
   CUtensorMap tm_v;  // [BH][Nk][D]
+  CUtensorMap tm_mask;  // staged mask kind: [B][mask_heads][Nq][Nk] fp32
 };
 static_assert(sizeof(Params) <= 4096, "kernel parameter space");
 
@@ -268,6 +310,7 @@ struct Barriers {
   uint32_t tmem_base;
   volatile int abort_flag;
   uint64_t kv_full[8], kv_empty[8];
+  uint64_t m_full[kMaskFullBars], m_empty[kMaskSlots];  // staged mask pieces
   int dbg_unit[3];  // debug builds: (unit, bh, q0) the producer loaded Q for
 };
 
@@ -374,19 +417,6 @@ __device__ __forceinline__ float2 exp2_fma_pipe(float2 x) {
   return make_float2(__uint_as_float(b0), __uint_as_float(b1));
 }
 
-// How the general softmax path reads additive mask values, one kind per
-// launch (chosen on the host from the mask, Nk and the alignment): none (only
-// the key-range checks), fp32 or uint8 values of one row read 16 bytes per
-// load (row starts 16-byte aligned), or one element per load.  The key-padding
-// mask [B][Nk] is a row shared by every query row of a batch entry.
-enum : int {
-  kMaskNone = 0,
-  kMaskF32Vec = 1,
-  kMaskF32Scalar = 2,
-  kMaskU8Vec = 3,
-  kMaskU8Scalar = 4,
-};
-
 // Mask values of one 16-key step of the general softmax path (keys
 // key0 .. key0 + 15 of the row `mrow`): 16 fp32 values, or 16 bytes packed
 // four to a word in w[0..3].  Every index is clamped inside the row (values
@@ -473,18 +503,80 @@ __device__ __forceinline__ float general_pass1(uint32_t tS, const void* mrow, in
   return mx;
 }
 
+// Pass 1 of the general path for a staged fp32 mask (kMaskF32Staged): as
+// general_pass1, with the row's mask values read from the shared-memory
+// pieces the mask producer filled.  A piece is 16 KB: 128 rows x 32 fp32
+// keys (128 bytes), 128-byte swizzle: 16-byte chunk c of row r sits at chunk
+// c ^ (r mod 8), so a warp's 32 rows read distinct bank groups.  Pieces
+// piece0 .. piece0 + 3 of the producer's sequence hold this block's keys for
+// this tile; piece i is in slot i mod kMaskSlots, signalled on full barrier
+// i mod kMaskFullBars.  Each is waited for, read (only its steps below
+// `nsteps`), and released by every warp of the warpgroup (one arrive per
+// warp).  Returns the row max; `ok` false if a wait ran out (the CTA is
+// aborting).
+__device__ __forceinline__ float general_pass1_staged(uint32_t tS, const uint8_t* sMask,
+                                                      Barriers* bars, const Params& p, int row,
+                                                      int lo, uint32_t span, float sl2, int nsteps,
+                                                      uint32_t piece0, bool& ok) {
+  constexpr float kLog2e = 1.4426950408889634f;
+  constexpr int PK = 32;                    // keys per piece
+  constexpr int NP = 128 / PK;              // pieces per block
+  constexpr int PB = 128 * 128;             // bytes per piece
+  constexpr int STEPS = PK / kGenStep;      // 16-key steps per piece
+  const uint32_t lane = threadIdx.x & 31;
+  const int rsw = row & 7;
+  float mx = -INFINITY;
+#pragma unroll 1
+  for (int pc = 0; pc < NP; ++pc) {
+    const uint32_t idx = piece0 + (uint32_t)pc;
+    if (!bounded_wait_warp(ptx::smem_u32(&bars->m_full[idx % kMaskFullBars]),
+                           (idx / kMaskFullBars) & 1u, bars, p.timeout_ns, p.status)) {
+      ok = false;
+      return mx;
+    }
+    const uint8_t* rowp = sMask + (idx % kMaskSlots) * PB + row * 128;
+#pragma unroll 1
+    for (int st = 0; st < STEPS; ++st) {
+      const int cb = pc * PK + st * kGenStep;
+      if (cb >= nsteps * kGenStep) break;
+      uint32_t w[kGenStep];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int c = st * 4 + i;  // 16-byte chunk of the 128-byte row
+        const uint4 v = *reinterpret_cast<const uint4*>(rowp + ((c ^ rsw) << 4));
+        w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+      }
+      uint32_t r[kGenStep];
+      ptx::tmem_ld32x32b_x16(tS + cb, r);
+      const int d = cb - lo;
+#pragma unroll
+      for (int i = 0; i < kGenStep; ++i) {
+        float t = fmaf(__uint_as_float(w[i]), kLog2e, __uint_as_float(r[i]) * sl2);
+        t = (uint32_t)(d + i) < span ? t : -INFINITY;
+        mx = fmaxf(mx, t);
+        r[i] = __float_as_uint(t);
+      }
+      ptx::tmem_st32x32b_x16(tS + cb, r);
+    }
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->m_empty[idx % kMaskSlots]));
+  }
+  return mx;
+}
+
 // MK: how the general softmax path reads mask values (kMask*).  Each kind is
 // its own instantiation, so a launch carries only the mask code it runs (the
 // kernel's speed is sensitive to its instruction footprint).
 template <int D, bool F8, int MK>
-__global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
+__global__ void __launch_bounds__(Cfg<D, F8, MK>::THREADS, 1)
     fa_fwd_kernel(const __grid_constant__ Params p) {
-  using C = Cfg<D, F8>;
+  using C = Cfg<D, F8, MK>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint8_t* sQ = smem;                      // 2 tiles
-  uint8_t* sRing = smem + C::SMEM_Q;       // STAGES tiles
+  uint8_t* sQ = smem;                          // 2 tiles
+  uint8_t* sMask = smem + C::SMEM_Q;           // staged mask kind: MASK_SLOTS pieces
+  uint8_t* sRing = sMask + C::SMEM_MASK;       // STAGES tiles
   Barriers* bars = reinterpret_cast<Barriers*>(sRing + C::SMEM_RING);
 
   const int warp = threadIdx.x / 32;
@@ -503,6 +595,11 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
     for (int s = 0; s < C::STAGES; ++s) {
       ptx::mbar_init(ptx::smem_u32(&bars->kv_full[s]), 1);
       ptx::mbar_init(ptx::smem_u32(&bars->kv_empty[s]), 1);
+    }
+    if constexpr (C::STAGED_MASK) {
+      for (int s = 0; s < C::MASK_FULL_BARS; ++s) ptx::mbar_init(ptx::smem_u32(&bars->m_full[s]), 1);
+      for (int s = 0; s < C::MASK_SLOTS; ++s)
+        ptx::mbar_init(ptx::smem_u32(&bars->m_empty[s]), 4);  // one arrive per consuming warp
     }
     bars->abort_flag = 0;
     ptx::fence_barrier_init();
@@ -766,6 +863,56 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
       }
     }
     __syncwarp();
+  } else if (warp == 10) {
+    // ----------------------------------------------- staged-mask producer --
+    // Walks the same units and key blocks as the K/V producer and copies, for
+    // every (key block, query tile), the mask pieces the softmax will read,
+    // in the order it reads them (block, tile, piece), through a ring of
+    // MASK_SLOTS shared-memory slots.
+    if constexpr (C::STAGED_MASK) {
+      if (lane == 0) {
+        ptx::tma_prefetch_desc(&p.tm_mask);
+        uint32_t mc = 0;  // pieces issued
+        bool ok = true;
+        for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+          const Unit un = decode_unit(p, u);
+          if (!fa_check(p, bars, unit_in_bounds(p, un), kCheckUnit, u, un.bh)) {
+            ok = false;
+            break;
+          }
+          const int b = (int)p.div_h.div((uint32_t)un.bh);
+          const int hm = p.mask_heads == 1 ? 0 : un.bh - b * p.H;
+          for (int j = 0; j < un.ntiles && ok; ++j)
+            for (int t = 0; t < un.nq && ok; ++t)
+              for (int pc = 0; pc < C::MASK_PIECES; ++pc, ++mc) {
+                const uint32_t slot = mc % C::MASK_SLOTS, ph = (mc / C::MASK_SLOTS) & 1u;
+                ok = bounded_wait(ptx::smem_u32(&bars->m_empty[slot]), ph ^ 1u, bars, p.timeout_ns,
+                                  p.status);
+                if (!ok) break;
+                const uint32_t fb = ptx::smem_u32(&bars->m_full[mc % C::MASK_FULL_BARS]);
+                ptx::mbar_arrive_expect_tx(fb, C::MASK_PIECE_BYTES);
+                ptx::tma_load_4d(ptx::smem_u32(sMask + slot * C::MASK_PIECE_BYTES), &p.tm_mask, fb,
+                                 (un.tile0 + j) * 128 + pc * C::MASK_PIECE_KEYS, un.q0 + t * 128, hm,
+                                 b);
+              }
+        }
+        {
+          // Wait (bounded) until every piece this thread issued has landed:
+          // after an abort the softmax no longer waits for them, and the CTA
+          // must not exit with copies into its shared memory in flight.
+          for (uint32_t fbi = 0; fbi < (uint32_t)C::MASK_FULL_BARS; ++fbi) {
+            const uint32_t n = mc > fbi ? (mc - 1 - fbi) / C::MASK_FULL_BARS + 1 : 0;
+            if (n == 0) continue;
+            const uint32_t bar = ptx::smem_u32(&bars->m_full[fbi]);
+            uint64_t t0 = ptx::global_timer_ns();
+            while (!ptx::mbar_try_wait(bar, (n - 1) & 1) &&
+                   ptx::global_timer_ns() - t0 < p.timeout_ns) {
+            }
+          }
+        }
+      }
+    }
+    __syncwarp();
   }
   finish();  // warps 8-11
   return;
@@ -786,11 +933,14 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
     const float scale_log2 = p.scale_log2;
     constexpr float kRescaleThreshold = 8.0f;  // log2 units: P stays <= 2^8
     uint32_t sc = 0, oc = 0;
+    uint32_t mpiece = 0;  // staged masks: pieces of the units before this one
     bool ok = true;
 
     for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
       const Unit un = decode_unit(p, u);
       const int bh = un.bh, q0 = un.q0;
+      const uint32_t unit_piece0 = mpiece;
+      mpiece += (uint32_t)(un.ntiles * un.nq * C::MASK_PIECES);
       if (t == 1 && un.nq < 2) continue;
       ok = __all_sync(0xffffffffu, fa_check(p, bars, unit_in_bounds(p, un), kCheckUnit, u, bh));
       if (!ok) break;
@@ -850,7 +1000,7 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
         if (MK == kMaskF32Vec && mask_b != nullptr)
           kv4 = __ldg(reinterpret_cast<const float4*>(mask_b + min(k4, p.Nk - 4)));
         uint32_t mwa[kGenStep], mwb[kGenStep];
-        if (MK != kMaskNone && (general_fixed || mask_b != nullptr)) {
+        if (MK != kMaskNone && !C::STAGED_MASK && (general_fixed || mask_b != nullptr)) {
           general_load<MK>(mrow, kbase, p.Nk, mwa);
           general_load<MK>(mrow, kbase + kGenStep, p.Nk, mwb);
         }
@@ -968,7 +1118,17 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
           // and m, l are unchanged.)
           const int hmax = __reduce_max_sync(0xffffffffu, span ? hi : 0);
           const int nsteps = blk_dead ? 0 : min(8, 2 * ((hmax + 31) / 32));
-          mx = general_pass1<MK>(tS, mrow, kbase, p.Nk, lo, span, sl2, nsteps, mwa, mwb);
+          if constexpr (C::STAGED_MASK) {
+            bool mok = true;
+            mx = general_pass1_staged(tS, sMask, bars, p, row, lo, span, sl2, nsteps,
+                                      unit_piece0 + (uint32_t)(j * un.nq + t) * C::MASK_PIECES, mok);
+            if (!__all_sync(0xffffffffu, mok)) {
+              ok = false;
+              break;
+            }
+          } else {
+            mx = general_pass1<MK>(tS, mrow, kbase, p.Nk, lo, span, sl2, nsteps, mwa, mwb);
+          }
           ptx::tmem_wait_st();  // pass 2 reads these columns back
           update_max(mx);
           // Pass 2 of the general path: exponentials of the log2-domain values
