@@ -57,6 +57,8 @@ enum : int {
   kMaskU8Scalar = 4,
   kMaskF32Staged = 5,
 };
+// Deepest K/V ring (barrier pairs reserved).
+constexpr int kMaxStages = 16;
 // Staged mask ring: slots of 16 KB (128 rows x 128 bytes) and the full
 // barriers that signal them (two per slot; the reason is given in Cfg).
 constexpr int kMaskSlots = 4;
@@ -96,6 +98,12 @@ struct Cfg {
 #ifndef FA_STAGES_D128
 #define FA_STAGES_D128 5
 #endif
+#ifndef FA_STAGES_D64
+#define FA_STAGES_D64 6
+#endif
+#ifndef FA_STAGES_D32
+#define FA_STAGES_D32 8
+#endif
   // Staged mask pieces: 16 KB each (128 rows x 32 fp32 keys, 128-byte
   // swizzle), a ring of MASK_SLOTS, MASK_PIECES per 128-key block per query
   // tile.
@@ -111,10 +119,13 @@ struct Cfg {
   static constexpr int MASK_PIECE_BYTES = 128 * 128;
   static constexpr int MASK_PIECE_KEYS = 32;
   static constexpr int MASK_PIECES = 128 / MASK_PIECE_KEYS;
-  // K/V ring depth: as deep as shared memory allows (227 KB per CTA).
-  static constexpr int STAGES = STAGED_MASK ? ((D == 128) ? 3 : (D == 64 ? 4 : 8))
+  // K/V ring depth (build options FA_STAGES_D*): at D = 128 as deep as
+  // shared memory allows (227 KB per CTA); at D <= 64 deeper rings (up to
+  // 12 / 16 stages fit) measured no faster than 6 / 8.
+  static constexpr int STAGES = STAGED_MASK ? ((D == 128) ? 3 : (D == 64 ? 8 : 16))
                                             : ((D == 128) ? (F8 ? 6 : FA_STAGES_D128)
-                                                          : (D == 64 ? 6 : 8));
+                                                          : (D == 64 ? FA_STAGES_D64 : FA_STAGES_D32));
+  static_assert(STAGES <= kMaxStages, "ring barriers");
   static constexpr int SMEM_Q = 2 * QK_TILE_BYTES;
   static constexpr int SMEM_MASK = STAGED_MASK ? MASK_SLOTS * MASK_PIECE_BYTES : 0;
   static constexpr int SMEM_RING = STAGES * TILE_BYTES;
@@ -129,6 +140,13 @@ struct Cfg {
   static constexpr uint32_t LAYOUT = (SW == 128) ? 2u : 4u;  // UMMA SWIZZLE_128B / SWIZZLE_64B
   static constexpr int TMEM_COLS = 512;
   static constexpr int COL_S0 = 0, COL_S1 = 128, COL_O0 = 256, COL_O1 = 256 + D;
+  // At D <= 64 the bf16 P of each tile (64 columns) has columns of its own,
+  // so S_t(j+1) can be computed while P_t(j) waits for its P·V MMAs; at
+  // D = 128 the 512 columns are full and P is written over S.
+  static constexpr bool SEP_P = D <= 64;
+  static constexpr int COL_P0 = SEP_P ? 256 + 2 * D : COL_S0;
+  static constexpr int COL_P1 = SEP_P ? 256 + 2 * D + 64 : COL_S1;
+  static_assert(!SEP_P || COL_P1 + 64 <= TMEM_COLS, "tensor-memory columns");
   static constexpr int THREADS = 384;
   // Launch: 168 registers x 384 threads.  The softmax warpgroups (0, 1)
   // rise to REGS_SOFTMAX, warpgroup 2 (producer, MMA, idle) drops to
@@ -306,10 +324,12 @@ __host__ __device__ constexpr uint32_t make_idesc_f8(int M, int N) {
 struct Barriers {
   uint64_t q_full, q_empty;
   uint64_t s_full[2], p_half[2], p_ready[2], o_full[2];
+  uint64_t s_free[2], pv_done[2];  // separate-P schedule (D <= 64)
+  uint64_t drain1;                 // the second MMA warp's drain (D <= 64)
   uint64_t drain;
   uint32_t tmem_base;
   volatile int abort_flag;
-  uint64_t kv_full[8], kv_empty[8];
+  uint64_t kv_full[kMaxStages], kv_empty[kMaxStages];
   uint64_t m_full[kMaskFullBars], m_empty[kMaskSlots];  // staged mask pieces
   int dbg_unit[3];  // debug builds: (unit, bh, q0) the producer loaded Q for
 };
@@ -584,17 +604,20 @@ __global__ void __launch_bounds__(Cfg<D, F8, MK>::THREADS, 1)
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(ptx::smem_u32(&bars->q_full), 1);
-    ptx::mbar_init(ptx::smem_u32(&bars->q_empty), 1);
+    ptx::mbar_init(ptx::smem_u32(&bars->q_empty), C::SEP_P ? 2 : 1);  // one per MMA warp
     for (int t = 0; t < 2; ++t) {
       ptx::mbar_init(ptx::smem_u32(&bars->s_full[t]), 1);
       ptx::mbar_init(ptx::smem_u32(&bars->p_half[t]), 128);
       ptx::mbar_init(ptx::smem_u32(&bars->p_ready[t]), 128);
       ptx::mbar_init(ptx::smem_u32(&bars->o_full[t]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bars->s_free[t]), 4);  // one arrive per softmax warp
+      ptx::mbar_init(ptx::smem_u32(&bars->pv_done[t]), 1);
     }
     ptx::mbar_init(ptx::smem_u32(&bars->drain), 1);
+    ptx::mbar_init(ptx::smem_u32(&bars->drain1), 1);
     for (int s = 0; s < C::STAGES; ++s) {
       ptx::mbar_init(ptx::smem_u32(&bars->kv_full[s]), 1);
-      ptx::mbar_init(ptx::smem_u32(&bars->kv_empty[s]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bars->kv_empty[s]), C::SEP_P ? 2 : 1);
     }
     if constexpr (C::STAGED_MASK) {
       for (int s = 0; s < C::MASK_FULL_BARS; ++s) ptx::mbar_init(ptx::smem_u32(&bars->m_full[s]), 1);
@@ -709,10 +732,13 @@ __global__ void __launch_bounds__(Cfg<D, F8, MK>::THREADS, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 9) {
+  } else if (warp == 9 || (C::SEP_P && warp == 11)) {
     // ----------------------------------------------------------------- MMA --
     // The whole warp runs the loop (operands warp-uniform); one elected lane
-    // issues each MMA batch and commit.
+    // issues each MMA batch and commit.  With separate P columns (D <= 64)
+    // two warps share the work: warp 9 issues tile 0's MMAs, warp 11 tile
+    // 1's (a single issuing warp spends more time per key block on its
+    // barrier waits, issues and commits than the softmax does at D <= 64).
     {
       constexpr uint32_t IDESC_QK = F8 ? make_idesc_f8(128, 128) : make_idesc(128, 128, false);
       constexpr uint32_t IDESC_PV = make_idesc(128, D, true);
@@ -766,12 +792,22 @@ __global__ void __launch_bounds__(Cfg<D, F8, MK>::THREADS, 1)
       constexpr uint32_t kVStep16 = (16 * C::SW) >> 4;
       auto issue_pv_half = [&](int t, uint32_t stg, int half, bool first) {
         const uint32_t b = dv_lo + stg * kTile16 + half * 4 * kVStep16;
-        const uint32_t a_tmem = tmem + (t ? C::COL_S1 : C::COL_S0) + half * 32;
+        const uint32_t a_tmem = tmem + (t ? C::COL_P1 : C::COL_P0) + half * 32;
         const uint32_t d = tmem + (t ? C::COL_O1 : C::COL_O0);
         ptx::mma_ts_x4_el<kVStep16>(d, a_tmem, b, dv_hi, IDESC_PV, first ? 0u : 1u);
       };
-      // Waits for each half of P_t, then issues its MMAs.
+      // Waits for each half of P_t, then issues its MMAs.  With separate P
+      // columns (not on the S critical path) P is released once and its 8
+      // MMAs go out together.
       auto issue_pv = [&](int t, uint32_t stg, bool first, uint32_t parity) -> bool {
+        if constexpr (C::SEP_P) {
+          if (!bounded_wait_warp(ptx::smem_u32(&bars->p_ready[t]), parity, bars, p.timeout_ns, p.status))
+            return false;
+          ptx::tc_fence_after_sync();
+          ptx::mma_ts_x8_el<kVStep16>(tmem + (t ? C::COL_O1 : C::COL_O0), tmem + (t ? C::COL_P1 : C::COL_P0),
+                                      dv_lo + stg * kTile16, dv_hi, IDESC_PV, first ? 0u : 1u);
+          return true;
+        }
         if (!bounded_wait_warp(ptx::smem_u32(&bars->p_half[t]), parity, bars, p.timeout_ns, p.status))
           return false;
         ptx::tc_fence_after_sync();
@@ -794,69 +830,151 @@ __global__ void __launch_bounds__(Cfg<D, F8, MK>::THREADS, 1)
         return r;
       };
 
-      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uc) {
-        const Unit un = decode_unit(p, u);
-        const bool has1 = un.nq == 2;
-        const int nkv = un.ntiles;
-        ok = bounded_wait_warp(ptx::smem_u32(&bars->q_full), uc & 1, bars, p.timeout_ns, p.status);
-        if (!ok) break;
+      if constexpr (C::SEP_P) {
+        // Separate-P schedule, one warp per tile (mt).  Per key block j:
+        // S_mt(j+1) as soon as the softmax warpgroup has read its S(j) into
+        // registers (s_free), so it is computed a block ahead; then
+        // P_mt(j) V once the softmax releases P.  Each P V is committed to
+        // pv_done[mt], which the softmax waits for before it writes P again
+        // (and before its epilogue reads O).  s_free phases: one per S tile
+        // the softmax has read; S tile number n (n >= 1) waits for phase n-1.
+        // K/V stages and the Q buffer are released by one arrival from each
+        // MMA warp; in units without a second tile warp 11 arrives without
+        // MMAs (after taking the stage, so it never runs a phase ahead).
+        const int mt = warp == 9 ? 0 : 1;
+        uint32_t ns = 0, pcm = 0;
+        auto release_stage = [&](uint32_t stg, bool mine) {
+          if (mine)
+            ptx::mma_commit_el(ptx::smem_u32(&bars->kv_empty[stg]));
+          else if (lane == 0)
+            ptx::mbar_arrive(ptx::smem_u32(&bars->kv_empty[stg]));
+        };
+        auto release_q = [&](bool mine) {
+          if (mine)
+            ptx::mma_commit_el(ptx::smem_u32(&bars->q_empty));
+          else if (lane == 0)
+            ptx::mbar_arrive(ptx::smem_u32(&bars->q_empty));
+        };
+        // S_mt for the key block in stage sK, after the softmax has read the
+        // previous S_mt.
+        auto next_s = [&](uint32_t sK) -> bool {
+          if (ns > 0) {
+            if (!bounded_wait_warp(ptx::smem_u32(&bars->s_free[mt]), (ns - 1) & 1, bars,
+                                   p.timeout_ns, p.status))
+              return false;
+            ptx::tc_fence_after_sync();
+          }
+          ++ns;
+          issue_s(mt, sK);
+          ptx::mma_commit_el(ptx::smem_u32(&bars->s_full[mt]));
+          return true;
+        };
+        for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uc) {
+          const Unit un = decode_unit(p, u);
+          const bool mine = mt == 0 || un.nq == 2;
+          const int nkv = un.ntiles;
+          ok = bounded_wait_warp(ptx::smem_u32(&bars->q_full), uc & 1, bars, p.timeout_ns, p.status);
+          if (!ok) break;
 #ifdef FA_DEBUG
-        ok = fa_check(p, bars, unit_in_bounds(p, un) && bars->dbg_unit[0] == u &&
-                                   bars->dbg_unit[1] == un.bh && bars->dbg_unit[2] == un.q0,
-                      kCheckUnitSync, u, bars->dbg_unit[0]);
-        if (!__all_sync(0xffffffffu, ok)) break;
+          if (mt == 0) {
+            ok = fa_check(p, bars, unit_in_bounds(p, un) && bars->dbg_unit[0] == u &&
+                                       bars->dbg_unit[1] == un.bh && bars->dbg_unit[2] == un.q0,
+                          kCheckUnitSync, u, bars->dbg_unit[0]);
+            if (!__all_sync(0xffffffffu, ok)) break;
+          }
 #endif
-        ptx::tc_fence_after_sync();
-        // Prologue: S for key block 0.
-        uint32_t sK = 0, sV = 0;
-        ok = take_stage(sK);
-        if (!ok) break;
-        issue_s(0, sK);
-        ptx::mma_commit_el(ptx::smem_u32(&bars->s_full[0]));
-        if (has1) {
-          issue_s(1, sK);
-          ptx::mma_commit_el(ptx::smem_u32(&bars->s_full[1]));
-        }
-        ptx::mma_commit_el(ptx::smem_u32(&bars->kv_empty[sK]));
-        if (nkv == 1) ptx::mma_commit_el(ptx::smem_u32(&bars->q_empty));
-
-        for (int j = 0; j < nkv && ok; ++j) {
-          ok = take_stage(sV);
+          ptx::tc_fence_after_sync();
+          uint32_t sK = 0, sV = 0;
+          ok = take_stage(sK) && (!mine || next_s(sK));
           if (!ok) break;
-          const bool has_next = j + 1 < nkv;
-          // O0 += P0 V_j
-          ok = issue_pv(0, sV, j == 0, pc0 & 1);
-          if (!ok) break;
-          ++pc0;
-          if (!has_next) ptx::mma_commit_el(ptx::smem_u32(&bars->o_full[0]));
-          // S0 for key block j+1 as soon as P0 has been consumed.
-          if (has_next) {
-            ok = take_stage(sK);
+          release_stage(sK, mine);
+          if (nkv == 1) release_q(mine);
+          for (int j = 0; j < nkv && ok; ++j) {
+            const bool has_next = j + 1 < nkv;
+            ok = take_stage(sV) && (!has_next || take_stage(sK));
             if (!ok) break;
-            issue_s(0, sK);
-            ptx::mma_commit_el(ptx::smem_u32(&bars->s_full[0]));
-          }
-          if (has1) {
-            ok = issue_pv(1, sV, j == 0, pc1 & 1);
-            if (!ok) break;
-            ++pc1;
-            if (!has_next) ptx::mma_commit_el(ptx::smem_u32(&bars->o_full[1]));
-          }
-          ptx::mma_commit_el(ptx::smem_u32(&bars->kv_empty[sV]));
-          if (has_next) {
-            if (has1) {
-              issue_s(1, sK);
-              ptx::mma_commit_el(ptx::smem_u32(&bars->s_full[1]));
+            if (has_next) {
+              if (mine) {
+                ok = next_s(sK);
+                if (!ok) break;
+              }
+              release_stage(sK, mine);
+              if (j + 2 == nkv) release_q(mine);
             }
-            ptx::mma_commit_el(ptx::smem_u32(&bars->kv_empty[sK]));
-            if (j + 2 == nkv) ptx::mma_commit_el(ptx::smem_u32(&bars->q_empty));
+            if (mine) {
+              ok = issue_pv(mt, sV, j == 0, pcm & 1);
+              if (!ok) break;
+              ++pcm;
+              ptx::mma_commit_el(ptx::smem_u32(&bars->pv_done[mt]));
+            }
+            release_stage(sV, mine);
+          }
+        }
+      } else {
+        for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uc) {
+          const Unit un = decode_unit(p, u);
+          const bool has1 = un.nq == 2;
+          const int nkv = un.ntiles;
+          ok = bounded_wait_warp(ptx::smem_u32(&bars->q_full), uc & 1, bars, p.timeout_ns, p.status);
+          if (!ok) break;
+  #ifdef FA_DEBUG
+          ok = fa_check(p, bars, unit_in_bounds(p, un) && bars->dbg_unit[0] == u &&
+                                     bars->dbg_unit[1] == un.bh && bars->dbg_unit[2] == un.q0,
+                        kCheckUnitSync, u, bars->dbg_unit[0]);
+          if (!__all_sync(0xffffffffu, ok)) break;
+  #endif
+          ptx::tc_fence_after_sync();
+          // Prologue: S for key block 0.
+          uint32_t sK = 0, sV = 0;
+          ok = take_stage(sK);
+          if (!ok) break;
+          issue_s(0, sK);
+          ptx::mma_commit_el(ptx::smem_u32(&bars->s_full[0]));
+          if (has1) {
+            issue_s(1, sK);
+            ptx::mma_commit_el(ptx::smem_u32(&bars->s_full[1]));
+          }
+          ptx::mma_commit_el(ptx::smem_u32(&bars->kv_empty[sK]));
+          if (nkv == 1) ptx::mma_commit_el(ptx::smem_u32(&bars->q_empty));
+
+          for (int j = 0; j < nkv && ok; ++j) {
+            ok = take_stage(sV);
+            if (!ok) break;
+            const bool has_next = j + 1 < nkv;
+            // O0 += P0 V_j
+            ok = issue_pv(0, sV, j == 0, pc0 & 1);
+            if (!ok) break;
+            ++pc0;
+            if (!has_next) ptx::mma_commit_el(ptx::smem_u32(&bars->o_full[0]));
+            // S0 for key block j+1 as soon as P0 has been consumed.
+            if (has_next) {
+              ok = take_stage(sK);
+              if (!ok) break;
+              issue_s(0, sK);
+              ptx::mma_commit_el(ptx::smem_u32(&bars->s_full[0]));
+            }
+            if (has1) {
+              ok = issue_pv(1, sV, j == 0, pc1 & 1);
+              if (!ok) break;
+              ++pc1;
+              if (!has_next) ptx::mma_commit_el(ptx::smem_u32(&bars->o_full[1]));
+            }
+            ptx::mma_commit_el(ptx::smem_u32(&bars->kv_empty[sV]));
+            if (has_next) {
+              if (has1) {
+                issue_s(1, sK);
+                ptx::mma_commit_el(ptx::smem_u32(&bars->s_full[1]));
+              }
+              ptx::mma_commit_el(ptx::smem_u32(&bars->kv_empty[sK]));
+              if (j + 2 == nkv) ptx::mma_commit_el(ptx::smem_u32(&bars->q_empty));
+            }
           }
         }
       }
       // Drain this thread's MMAs before tensor memory can be freed.
-      ptx::mma_commit_el(ptx::smem_u32(&bars->drain));
       {
-        const uint32_t bar = ptx::smem_u32(&bars->drain);
+        const uint32_t bar = ptx::smem_u32(warp == 9 ? &bars->drain : &bars->drain1);
+        ptx::mma_commit_el(bar);
         uint64_t t0 = ptx::global_timer_ns();
         while (!ptx::mbar_try_wait(bar, 0) && ptx::global_timer_ns() - t0 < p.timeout_ns) {
         }
@@ -926,13 +1044,34 @@ __global__ void __launch_bounds__(Cfg<D, F8, MK>::THREADS, 1)
     const uint32_t lane_base = (uint32_t)((warp % 4) * 32) << 16;
     const uint32_t tS = tmem + lane_base + (t ? C::COL_S1 : C::COL_S0);
     const uint32_t tO = tmem + lane_base + (t ? C::COL_O1 : C::COL_O0);
+    const uint32_t tP = tmem + lane_base + (t ? C::COL_P1 : C::COL_P0);
+    const uint32_t bar_sf = ptx::smem_u32(&bars->s_free[t]);
+    const uint32_t bar_pv = ptx::smem_u32(&bars->pv_done[t]);
     const uint32_t bar_s = ptx::smem_u32(&bars->s_full[t]);
     const uint32_t bar_ph = ptx::smem_u32(&bars->p_half[t]);
     const uint32_t bar_p = ptx::smem_u32(&bars->p_ready[t]);
     const uint32_t bar_o = ptx::smem_u32(&bars->o_full[t]);
     const float scale_log2 = p.scale_log2;
     constexpr float kRescaleThreshold = 8.0f;  // log2 units: P stays <= 2^8
-    uint32_t sc = 0, oc = 0;
+    uint32_t sc = 0, oc = 0, pvc = 0;
+    // Separate-P schedule (D <= 64): S_t has been read (the MMA may write the
+    // next S_t), and wait until the last P_t V has consumed P_t (before P_t is
+    // written again, O_t rescaled or read by the epilogue).
+    auto free_s = [&]() {
+      if constexpr (C::SEP_P) {
+        ptx::tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(bar_sf);
+      }
+    };
+    auto wait_pv = [&]() -> bool {
+      if constexpr (C::SEP_P) {
+        if (!bounded_wait_warp(bar_pv, pvc & 1, bars, p.timeout_ns, p.status)) return false;
+        ++pvc;
+        ptx::tc_fence_after_sync();
+      }
+      return true;
+    };
     uint32_t mpiece = 0;  // staged masks: pieces of the units before this one
     bool ok = true;
 
@@ -1046,11 +1185,12 @@ __global__ void __launch_bounds__(Cfg<D, F8, MK>::THREADS, 1)
           }
           m_use = (m == -INFINITY) ? 0.f : m;
           l *= alpha;
-          // P in two halves of 64 keys, each released as soon as it is in
-          // tensor memory so the first P·V MMAs overlap the second half's exp2.
-          // When O must be rescaled (rare: the max grew past the threshold) the
-          // first half waits until all of P is stored, so that the rescale runs
-          // with the scores already consumed.
+          // At D = 128, P in two halves of 64 keys, each released as soon as
+          // it is in tensor memory so the first P·V MMAs overlap the second
+          // half's exp2 (with separate P columns, P is released whole).  When
+          // O must be rescaled (rare: the max grew past the threshold) the
+          // first half waits until all of P is stored, so that the rescale
+          // runs with the scores already consumed.
           rescale_o = j > 0 && __any_sync(0xffffffffu, grow);
         };
         float2 lsum = make_float2(0.f, 0.f);
@@ -1063,6 +1203,7 @@ __global__ void __launch_bounds__(Cfg<D, F8, MK>::THREADS, 1)
 #pragma unroll
             for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(r[c]);
           }
+          free_s();
           float a0 = s[0], a1 = s[1], a2 = s[2], a3 = s[3];
 #pragma unroll
           for (int c = 4; c < 128; c += 8) {
@@ -1073,6 +1214,10 @@ __global__ void __launch_bounds__(Cfg<D, F8, MK>::THREADS, 1)
           }
           mx = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)) * sl2;
           update_max(mx);
+          if (j > 0 && !wait_pv()) {
+            ok = false;
+            break;
+          }
           const float2 sc2 = make_float2(sl2, sl2);
           const float2 nm2 = make_float2(-m_use, -m_use);
 #pragma unroll
@@ -1091,8 +1236,8 @@ __global__ void __launch_bounds__(Cfg<D, F8, MK>::THREADS, 1)
               lsum = __fadd2_rn(lsum, pr);
               packed[c / 2] = ptx::pack_bf16x2(pr.x, pr.y);
             }
-            ptx::tmem_st32x32b_x16(tS + cb / 2, packed);
-            if (cb == 32 && !rescale_o) release(0);
+            ptx::tmem_st32x32b_x16(tP + cb / 2, packed);
+            if (!C::SEP_P && cb == 32 && !rescale_o) release(0);
           }
         } else {
           float mx;
@@ -1131,10 +1276,15 @@ __global__ void __launch_bounds__(Cfg<D, F8, MK>::THREADS, 1)
           }
           ptx::tmem_wait_st();  // pass 2 reads these columns back
           update_max(mx);
+          if (j > 0 && !wait_pv()) {
+            ok = false;
+            break;
+          }
           // Pass 2 of the general path: exponentials of the log2-domain values
-          // pass 1 left in tensor memory; P (bf16 pairs) goes over the first 64
-          // columns, behind the columns still to be read.  Columns past the
-          // steps pass 1 processed are excluded for every row: P = 0 there.
+          // pass 1 left in tensor memory; P (bf16 pairs) goes to P's columns
+          // (at D = 128 the first 64 columns of S, behind the columns still to
+          // be read).  Columns past the steps pass 1 processed are excluded
+          // for every row: P = 0 there.
 #pragma unroll 1
           for (int cb = 0; cb < 128; cb += 32) {
             uint32_t packed[16];
@@ -1152,14 +1302,15 @@ __global__ void __launch_bounds__(Cfg<D, F8, MK>::THREADS, 1)
 #pragma unroll
               for (int c = 0; c < 16; ++c) packed[c] = 0u;
             }
-            ptx::tmem_st32x32b_x16(tS + cb / 2, packed);
-            if (cb == 32 && !rescale_o) release(0);
+            ptx::tmem_st32x32b_x16(tP + cb / 2, packed);
+            if (!C::SEP_P && cb == 32 && !rescale_o) release(0);
           }
+          free_s();
         }
         l += lsum.x + lsum.y;
         if (rescale_o) {
           // P(j-1)·V has landed: the S commit that released this iteration
-          // follows it.
+          // follows it (separate P: pv_done was waited for above).
 #pragma unroll
           for (int cb = 0; cb < D; cb += 32) {
             uint32_t r[32];
@@ -1168,16 +1319,20 @@ __global__ void __launch_bounds__(Cfg<D, F8, MK>::THREADS, 1)
             for (int c = 0; c < 32; ++c) r[c] = __float_as_uint(__uint_as_float(r[c]) * alpha);
             ptx::tmem_st32x32b_x32(tO + cb, r);
           }
-          release(0);
+          if constexpr (!C::SEP_P) release(0);
         }
         release(1);
       }
       if (!ok) break;
 
       // Epilogue: O / l -> bf16, LSE = ln2 * (m + log2 l).
-      ok = bounded_wait_warp(bar_o, oc & 1, bars, p.timeout_ns, p.status);
+      if constexpr (C::SEP_P) {
+        ok = wait_pv();  // the last P V of the unit: O is complete
+      } else {
+        ok = bounded_wait_warp(bar_o, oc & 1, bars, p.timeout_ns, p.status);
+        ++oc;
+      }
       if (!ok) break;
-      ++oc;
       ptx::tc_fence_after_sync();
       const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
       const bool valid_row = qrow < p.Nq;
