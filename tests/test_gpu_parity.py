@@ -70,6 +70,9 @@ def test_key_padding_mask(D, Nk):
     m = torch.where(cols[None] < valid[:, None], 0.0, float("-inf"))
     m[0, 3] = -1.25          # a finite additive entry
     m[1, 0] = 0.5
+    # batch entry 2: a distinct finite value on every valid key (a key-to-lane
+    # mix-up in the vector path changes the result)
+    m[2, : Nk - 1] = torch.linspace(-2.0, 1.5, Nk - 1)
     inp["mask"] = m.to(torch.float32).cuda().contiguous()
     inp["scale"] = float(np.float32(D ** -0.5))
     out, lse = run_gpu(inp)

@@ -37,7 +37,7 @@ int launch_one(const Params& prm, int device, int sm_count, cudaStream_t stream)
     }
   }
   const int grid = prm.num_units < sm_count ? prm.num_units : sm_count;
-  static const char* kMaskNames[] = {"none", "fp32x4", "fp32", "u8x16", "u8",
+  static const char* kMaskNames[] = {"none", "key fp32x4", "fp32", "u8x16", "u8",
                                       "fp32 staged"};
   log_launch("fa_fwd_kernel<D=%d,%s,mask %s> tile %dx%d grid %d x %d threads smem %d B tmem %d cols "
              "stages %d units %d (single-tile from %d) key ranges %d BH %d Nq %d Nk %d "

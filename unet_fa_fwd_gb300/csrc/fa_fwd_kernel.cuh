@@ -42,16 +42,22 @@ constexpr uint32_t kSuspendNs = 20000;  // longest sleep inside one mbarrier pol
 
 
 // How the general softmax path reads additive mask values, one kind per
-// launch (chosen on the host from the mask, Nk and the alignment): none (only
-// the key-range checks), fp32 or uint8 values of one row read 16 bytes per
-// load (row starts 16-byte aligned), or one element per load.  The key-padding
-// mask [B][Nk] is a row shared by every query row of a batch entry.  The
-// staged kind (a per-(query, key) fp32 mask whose rows are 16-byte multiples)
-// is copied by TMA into shared memory in 16 KB pieces of 128 rows x 32 keys by
-// a producer warp, ahead of the softmax.
+// launch (chosen on the host from the mask, Nk and the alignment):
+//   none          only the key-range checks;
+//   key fp32 x4   a key-padding mask [B][Nk] (one row shared by every query
+//                 row of a batch entry) with Nk a multiple of 4: each lane
+//                 loads 4 of a key block's 128 values before S is ready, and
+//                 the general path takes them from the lanes by shuffles;
+//   fp32 / u8     one element per load (rows not 16-byte aligned, or a
+//                 key-padding mask with Nk not a multiple of 4);
+//   u8 x16        a per-(query, key) byte mask, 16 bytes per load;
+//   fp32 staged   a per-(query, key) fp32 mask whose rows are 16-byte
+//                 multiples, copied by TMA into shared memory in 16 KB pieces
+//                 of 128 rows x 32 keys by a producer warp, ahead of the
+//                 softmax.
 enum : int {
   kMaskNone = 0,
-  kMaskF32Vec = 1,
+  kMaskF32Vec = 1,  // key fp32 x4
   kMaskF32Scalar = 2,
   kMaskU8Vec = 3,
   kMaskU8Scalar = 4,
@@ -122,16 +128,21 @@ struct Cfg {
   // K/V ring depth (build options FA_STAGES_D*): at D = 128 as deep as
   // shared memory allows (227 KB per CTA); at D <= 64 deeper rings (up to
   // 12 / 16 stages fit) measured no faster than 6 / 8.
-  static constexpr int STAGES = STAGED_MASK ? ((D == 128) ? 3 : (D == 64 ? 8 : 16))
+  static constexpr int STAGES = STAGED_MASK ? ((D == 128) ? 3 : (D == 64 ? 6 : 16))
                                             : ((D == 128) ? (F8 ? 6 : FA_STAGES_D128)
                                                           : (D == 64 ? FA_STAGES_D64 : FA_STAGES_D32));
   static_assert(STAGES <= kMaxStages, "ring barriers");
   static constexpr int SMEM_Q = 2 * QK_TILE_BYTES;
   static constexpr int SMEM_MASK = STAGED_MASK ? MASK_SLOTS * MASK_PIECE_BYTES : 0;
   static constexpr int SMEM_RING = STAGES * TILE_BYTES;
+  // D <= 64: each softmax warp stages its 32 output rows here for coalesced
+  // stores (at D = 128 shared memory is full; the epilogue shuffles).
+  static constexpr bool EPI_SMEM = D <= 64;
+  static constexpr int EPI_WARP_BYTES = 32 * D * 2;
+  static constexpr int SMEM_EPI = EPI_SMEM ? 8 * EPI_WARP_BYTES : 0;
   static constexpr int SMEM_BAR = 1024;
   static constexpr int SMEM_USED =
-      1024 /*align slack*/ + SMEM_Q + SMEM_MASK + SMEM_RING + SMEM_BAR;
+      1024 /*align slack*/ + SMEM_Q + SMEM_MASK + SMEM_RING + SMEM_EPI + SMEM_BAR;
   // 512 TMEM columns per CTA => one CTA per SM; pad shared memory so that a
   // second CTA never lands on the SM and blocks in tcgen05.alloc.
   static constexpr int SMEM_BYTES = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;
@@ -447,13 +458,7 @@ __device__ __forceinline__ void general_load(const void* mrow, int key0, int Nk,
                                              uint32_t (&w)[kGenStep]) {
   const float* mf = static_cast<const float*>(mrow);
   const uint8_t* mb = static_cast<const uint8_t*>(mrow);
-  if constexpr (MK == kMaskF32Vec) {
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(mf + min(key0 + 4 * k, Nk - 4)));
-      w[4 * k] = v.x; w[4 * k + 1] = v.y; w[4 * k + 2] = v.z; w[4 * k + 3] = v.w;
-    }
-  } else if constexpr (MK == kMaskF32Scalar) {
+  if constexpr (MK == kMaskF32Scalar) {
 #pragma unroll
     for (int i = 0; i < kGenStep; ++i) w[i] = __float_as_uint(__ldg(mf + min(key0 + i, Nk - 1)));
   } else if constexpr (MK == kMaskU8Vec) {
@@ -497,7 +502,7 @@ __device__ __forceinline__ float general_pass1(uint32_t tS, const void* mrow, in
     for (int i = 0; i < kGenStep; ++i) {
       float t = __uint_as_float(r[i]) * sl2;
       bool keep = (uint32_t)(d + i) < span;
-      if constexpr (MK == kMaskF32Vec || MK == kMaskF32Scalar) {
+      if constexpr (MK == kMaskF32Scalar) {
         t = fmaf(__uint_as_float(w[i]), kLog2e, t);
       } else if constexpr (MK == kMaskU8Vec || MK == kMaskU8Scalar) {
         keep = keep && ((w[i / 4] >> (8 * (i % 4))) & 0xffu) != 0u;
@@ -519,6 +524,41 @@ __device__ __forceinline__ float general_pass1(uint32_t tS, const void* mrow, in
     general_load<MK>(mrow, nb, Nk, a);
     step(cb + kGenStep, b);
     general_load<MK>(mrow, nb + kGenStep, Nk, b);
+  }
+  return mx;
+}
+
+// Pass 1 of the general path for a key-padding mask with Nk a multiple of 4
+// (kMaskF32Vec): as general_pass1, with the block's 128 mask values already
+// in registers across the warp (lane l holds keys 4l .. 4l + 3 of the block
+// in kv; clamped inside the row, so lanes past Nk hold values the key range
+// excludes).  Every row of the warp reads the same keys, so each 32-key step
+// takes its values by shuffles from lanes cb/4 .. cb/4 + 7.
+__device__ __forceinline__ float general_pass1_key4(uint32_t tS, float4 kv, int lo, uint32_t span,
+                                                    float sl2, int nsteps) {
+  constexpr float kLog2e = 1.4426950408889634f;
+  float mx = -INFINITY;
+  const int end = nsteps * kGenStep;  // nsteps is even: 32 keys per iteration
+#pragma unroll 1
+  for (int cb = 0; cb < end; cb += 2 * kGenStep) {
+    uint32_t r[2 * kGenStep];
+    ptx::tmem_ld32x32b_x32(tS + cb, r);
+    const int d = cb - lo;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int src = (cb >> 2) + q;
+      const float mv[4] = {__shfl_sync(0xffffffffu, kv.x, src), __shfl_sync(0xffffffffu, kv.y, src),
+                           __shfl_sync(0xffffffffu, kv.z, src), __shfl_sync(0xffffffffu, kv.w, src)};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i = 4 * q + e;
+        float t = fmaf(mv[e], kLog2e, __uint_as_float(r[i]) * sl2);
+        t = (uint32_t)(d + i) < span ? t : -INFINITY;
+        mx = fmaxf(mx, t);
+        r[i] = __float_as_uint(t);
+      }
+    }
+    ptx::tmem_st32x32b_x32(tS + cb, r);
   }
   return mx;
 }
@@ -597,7 +637,8 @@ __global__ void __launch_bounds__(Cfg<D, F8, MK>::THREADS, 1)
   uint8_t* sQ = smem;                          // 2 tiles
   uint8_t* sMask = smem + C::SMEM_Q;           // staged mask kind: MASK_SLOTS pieces
   uint8_t* sRing = sMask + C::SMEM_MASK;       // STAGES tiles
-  Barriers* bars = reinterpret_cast<Barriers*>(sRing + C::SMEM_RING);
+  uint8_t* sEpi = sRing + C::SMEM_RING;       // D <= 64: output staging, 8 warps
+  Barriers* bars = reinterpret_cast<Barriers*>(sEpi + C::SMEM_EPI);
 
   const int warp = threadIdx.x / 32;
   const uint32_t lane = threadIdx.x % 32;
@@ -1139,7 +1180,8 @@ __global__ void __launch_bounds__(Cfg<D, F8, MK>::THREADS, 1)
         if (MK == kMaskF32Vec && mask_b != nullptr)
           kv4 = __ldg(reinterpret_cast<const float4*>(mask_b + min(k4, p.Nk - 4)));
         uint32_t mwa[kGenStep], mwb[kGenStep];
-        if (MK != kMaskNone && !C::STAGED_MASK && (general_fixed || mask_b != nullptr)) {
+        if (MK != kMaskNone && MK != kMaskF32Vec && !C::STAGED_MASK &&
+            (general_fixed || mask_b != nullptr)) {
           general_load<MK>(mrow, kbase, p.Nk, mwa);
           general_load<MK>(mrow, kbase + kGenStep, p.Nk, mwb);
         }
@@ -1271,6 +1313,8 @@ __global__ void __launch_bounds__(Cfg<D, F8, MK>::THREADS, 1)
               ok = false;
               break;
             }
+          } else if constexpr (MK == kMaskF32Vec) {
+            mx = general_pass1_key4(tS, kv4, lo, span, sl2, nsteps);
           } else {
             mx = general_pass1<MK>(tS, mrow, kbase, p.Nk, lo, span, sl2, nsteps, mwa, mwb);
           }
@@ -1342,7 +1386,50 @@ __global__ void __launch_bounds__(Cfg<D, F8, MK>::THREADS, 1)
         // K was smoothed by its per-channel mean: add back scale * q_i . mean(K).
         if (valid_row) row_lse += __ldg(p.lse_corr + (size_t)bh * p.Nq + qrow);
       }
-      if (p.part_o == nullptr) {
+      if (p.part_o == nullptr && C::EPI_SMEM) {
+        // Coalesced stores through shared memory: each thread writes its
+        // row's D bf16 into the warp's staging buffer (16-byte chunk c of
+        // row r at chunk c ^ (r mod CH), so the 32 rows' writes and the
+        // reads below each take the minimum number of wavefronts), then
+        // each store instruction writes 32 / CH whole rows.
+        constexpr int CH = D * 2 / 16;  // 16-byte chunks per row
+        uint8_t* wbuf = sEpi + warp * C::EPI_WARP_BYTES;
+#pragma unroll
+        for (int cb = 0; cb < D; cb += 32) {
+          uint32_t r[32];
+          ptx::tmem_ld32x32b_x32(tO + cb, r);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint4 v = make_uint4(
+                ptx::pack_bf16x2(__uint_as_float(r[8 * q]) * inv_l, __uint_as_float(r[8 * q + 1]) * inv_l),
+                ptx::pack_bf16x2(__uint_as_float(r[8 * q + 2]) * inv_l, __uint_as_float(r[8 * q + 3]) * inv_l),
+                ptx::pack_bf16x2(__uint_as_float(r[8 * q + 4]) * inv_l, __uint_as_float(r[8 * q + 5]) * inv_l),
+                ptx::pack_bf16x2(__uint_as_float(r[8 * q + 6]) * inv_l, __uint_as_float(r[8 * q + 7]) * inv_l));
+            const int c = cb / 8 + q;
+            *reinterpret_cast<uint4*>(wbuf + lane * (D * 2) + ((c ^ (lane & (CH - 1))) << 4)) = v;
+          }
+        }
+        __syncwarp();
+        const int warp_row0 = q0 + t * 128 + (warp % 4) * 32;  // query row of lane 0
+#pragma unroll
+        for (int it = 0; it < CH; ++it) {
+          const int rr = it * (32 / CH) + (int)lane / CH;  // row within the warp's 32
+          const int c = (int)lane % CH;
+          const uint4 v = *reinterpret_cast<const uint4*>(wbuf + rr * (D * 2) + ((c ^ (rr & (CH - 1))) << 4));
+          const int orow = warp_row0 + rr;
+#ifdef FA_DEBUG
+          const int nq_bound = p.debug_plant ? p.Nq - 1 : p.Nq;
+          if (orow < p.Nq && fa_check(p, bars, orow < nq_bound && bh < p.BH, kCheckStore,
+                                      (long long)bh * p.Nq + orow, c))
+#else
+          if (orow < p.Nq)
+#endif
+            *reinterpret_cast<uint4*>(p.out + ((size_t)bh * p.Nq + orow) * D + c * 8) = v;
+        }
+        __syncwarp();  // the buffer is written again in the next unit
+        if (valid_row && fa_check(p, bars, bh < p.BH, kCheckStore, (long long)bh * p.Nq + qrow, -1))
+          p.lse[(size_t)bh * p.Nq + qrow] = row_lse;
+      } else if (p.part_o == nullptr) {
         // Coalesced stores: thread = row in tensor memory, so each 32-column
         // chunk (16 bf16 pairs per row) is transposed across the warp with
         // shuffles; in pass q, lanes 4i..4i+3 write row 8q + i's 64 bytes as
