@@ -1146,6 +1146,15 @@ __global__ void __launch_bounds__(Cfg<D, F8, MK>::THREADS, 1)
       if (mask_b != nullptr &&
           !fa_check(p, bars, b_idx >= 0 && b_idx < p.BH / p.H, kCheckMaskRow, b_idx, bh))
         mask_b = p.mask;
+      // Key-padding values (four keys per lane) of the unit's first key
+      // block, loaded now so that their latency overlaps the unit's set-up;
+      // each later block's are loaded one block ahead.
+      auto load_kv = [&](int blk) {
+        return __ldg(reinterpret_cast<const float4*>(
+            mask_b + min((un.tile0 + blk) * 128 + 4 * (int)lane, p.Nk - 4)));
+      };
+      float4 kv_next = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (MK == kMaskF32Vec && mask_b != nullptr) kv_next = load_kv(0);
       // Keys of this row's segment (all keys when rows are not segmented).
       const int seg_lo = p.seg > 0 ? (qrow / p.seg) * p.seg : 0;
       const int seg_hi = p.seg > 0 ? seg_lo + p.seg : INT_MAX;
@@ -1173,12 +1182,11 @@ __global__ void __launch_bounds__(Cfg<D, F8, MK>::THREADS, 1)
         const bool general_fixed = any_full_mask || (kbase + 128 > p.Nk) || !(sl2 >= 0.f) ||
                                    (p.causal && kbase + 127 > tile_row0) || p.seg > 0;
         // Loads issued before S is ready, so that their latency overlaps the
-        // wait: the key-padding values this lane classifies (four keys) and
-        // the general path's first two steps of mask values.
-        float4 kv4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        // wait: the next block's key-padding values, and the general path's
+        // first two steps of mask values.
+        const float4 kv4 = kv_next;  // this lane's four keys of this block
         const int k4 = kbase + 4 * (int)lane;
-        if (MK == kMaskF32Vec && mask_b != nullptr)
-          kv4 = __ldg(reinterpret_cast<const float4*>(mask_b + min(k4, p.Nk - 4)));
+        if (MK == kMaskF32Vec && mask_b != nullptr && j + 1 < un.ntiles) kv_next = load_kv(j + 1);
         uint32_t mwa[kGenStep], mwb[kGenStep];
         if (MK != kMaskNone && MK != kMaskF32Vec && !C::STAGED_MASK &&
             (general_fixed || mask_b != nullptr)) {
