@@ -498,17 +498,9 @@ def bench_native(args, world, rank, local):
 
     if args.also and rank == 0:
         ext = {}
-        # causal at the benchmark shape: the useful FLOPs count keys j <= i only
-        oc_, lc_ = torch.empty_like(q), torch.empty_like(lse)
-        msc = time_call(lambda: fa.fa_fwd_ex(q, k, v, oc_, lc_, causal=True, scale=inp["scale"],
-                                             stream=stream), max(5, args.steps // 10))
-        kept = (Nq * (Nq + 1) // 2 if Nq <= Nk          # sum over rows i of min(i + 1, Nk)
-                else Nk * (Nk + 1) // 2 + (Nq - Nk) * Nk)
-        cfl = 4.0 * B * H * D * kept
-        ext["causal"] = {"workload": args.workload, "ms_per_step": round(msc, 4),
-                         "tflops_useful": round(cfl / msc / 1e9, 1),
-                         "note": "FLOPs of the unmasked (j <= i) pairs only"}
-        del oc_, lc_
+        # The short masked and window timings first, after a pause that lets the
+        # clocks recover from the legs before (the long causal run heats the GPU).
+        time.sleep(2.0)
         # additive fp32 mask [B, 1, Nq, Nk] (broadcast over heads) at FLUX 1024^2
         wm = workloads.make_inputs("flux_1024", device=device)
         mB, mH, mNq, mNk, mD = wm["shape"]
@@ -516,13 +508,15 @@ def bench_native(args, world, rank, local):
         fmask = torch.randn((mB, 1, mNq, mNk), generator=g, device=device, dtype=torch.float32)
         om_ = torch.empty_like(wm["q"])
         lm_ = torch.empty((mB, mH, mNq), dtype=torch.float32, device=device)
-        msm = time_call(lambda: fa.fa_fwd_ex(wm["q"], wm["k"], wm["v"], om_, lm_, full_mask=fmask,
-                                             scale=wm["scale"], stream=stream), 20)
+        with ClockSampler(local) as mclocks:
+            msm = time_call(lambda: fa.fa_fwd_ex(wm["q"], wm["k"], wm["v"], om_, lm_, full_mask=fmask,
+                                                 scale=wm["scale"], stream=stream), 20)
         ext["additive_mask"] = {"workload": "flux_1024", "mask": "fp32 [B,1,Nq,Nk] N(0,1)",
                                 "ms_per_step": round(msm, 4),
                                 "tflops": round(accounting.attention_flops(mB, mH, mNq, mNk, mD)
                                                 / msm / 1e9, 1),
-                                "mask_mb": round(fmask.numel() * 4 / 1e6, 1)}
+                                "mask_mb": round(fmask.numel() * 4 / 1e6, 1),
+                                "clocks": mclocks.summary()}
         del wm, fmask, om_, lm_
         # window / shifted-window attention on the SD 512^2 latent grid (64 x 64 tokens)
         ww = workloads.make_inputs("sd_self", device=device)
@@ -538,6 +532,17 @@ def bench_native(args, world, rank, local):
                          "note": "gather + attention + scatter kernels, outputs allocated by the "
                                  "binding", "configs": win}
         del ww
+        # causal at the benchmark shape: the useful FLOPs count keys j <= i only
+        oc_, lc_ = torch.empty_like(q), torch.empty_like(lse)
+        msc = time_call(lambda: fa.fa_fwd_ex(q, k, v, oc_, lc_, causal=True, scale=inp["scale"],
+                                             stream=stream), max(5, args.steps // 10))
+        kept = (Nq * (Nq + 1) // 2 if Nq <= Nk          # sum over rows i of min(i + 1, Nk)
+                else Nk * (Nk + 1) // 2 + (Nq - Nk) * Nk)
+        cfl = 4.0 * B * H * D * kept
+        ext["causal"] = {"workload": args.workload, "ms_per_step": round(msc, 4),
+                         "tflops_useful": round(cfl / msc / 1e9, 1),
+                         "note": "FLOPs of the unmasked (j <= i) pairs only"}
+        del oc_, lc_
         also["masks_causal_window"] = ext
 
     # ---- FP8 (e4m3 Q K^T) forward on the same workload, pre-pass included ----
