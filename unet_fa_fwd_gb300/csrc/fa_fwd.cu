@@ -580,6 +580,9 @@ int fa_fwd_window(const void* q, const void* k, const void* v, void* out, float*
     while (pk > 1 && ((long long)B * nw) % pk) --pk;
     g.pack = pk;
   }
+  // Windowed rows are indexed in 32 bits (multiply-shift division).
+  if (rows >= (size_t(1) << 31)) return FA_ERR_INVALID_ARGUMENT;
+  g.finish();
   const long long chunks = (long long)rows * (D / 8);
   const long long blocks = (chunks + 255) / 256;
   if (blocks > INT_MAX) return FA_ERR_INVALID_ARGUMENT;
