@@ -80,11 +80,13 @@ __global__ void fa_k_mean_kernel(const float* __restrict__ partial, float* __res
 // chunks (8 elements), chunk i by thread i mod 256, so a warp's
 // loads and its 8-byte e4m3 stores cover whole rows contiguously.  A thread
 // always holds the same 8 channels (256 is a multiple of the chunks per row),
-// so it keeps their means in registers.  K: smoothed by the mean
-// first.  Q: also writes lse_corr = scale * (q_i . mean_k), reduced across the
-// D/8 lanes holding a row.
+// so it keeps their means in registers.  The block stays in registers as bf16
+// (converted to fp32 twice: for the block max, then to quantise), so four
+// CTAs fit an SM (three at D = 128) and more of the stream is in flight.  K: smoothed by the
+// mean first.  Q: also writes lse_corr = scale * (q_i . mean_k), reduced
+// across the D/8 lanes holding a row.
 template <int D>
-__global__ void __launch_bounds__(256, 2) fa_quant_kernel(
+__global__ void __launch_bounds__(256, D == 128 ? 3 : 4) fa_quant_kernel(
     const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ q,
     const float* __restrict__ mean_k, uint8_t* __restrict__ k8,
     uint8_t* __restrict__ q8, float* __restrict__ k_scale, float* __restrict__ q_scale,
@@ -117,26 +119,30 @@ __global__ void __launch_bounds__(256, 2) fa_quant_kernel(
     const int r = (i * 256 + tid) / PARTS;
     raw[i] = blk * 128 + r < N ? __ldg(src + i * 256 + tid) : make_uint4(0u, 0u, 0u, 0u);
   }
-  // fp32 values of the chunks (smoothed for K; rows past N are zero)
-  float val[PER][8];
-  float amax = 0.f;
-#pragma unroll
-  for (int i = 0; i < PER; ++i) {
+  // fp32 values of chunk i (smoothed for K; rows past N are zero)
+  auto values = [&](int i, float (&val)[8]) {
     const int r = (i * 256 + tid) / PARTS;
     const bool smooth = is_k && blk * 128 + r < N;
     const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&raw[i]);
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const float2 f = __bfloat1622float2(h2[e]);
-      val[i][2 * e] = smooth ? f.x - mean[2 * e] : f.x;
-      val[i][2 * e + 1] = smooth ? f.y - mean[2 * e + 1] : f.y;
+      val[2 * e] = smooth ? f.x - mean[2 * e] : f.x;
+      val[2 * e + 1] = smooth ? f.y - mean[2 * e + 1] : f.y;
     }
+  };
+  float amax = 0.f;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(val[i][e]));
+  for (int i = 0; i < PER; ++i) {
+    float val[8];
+    values(i, val);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(val[e]));
     if (!is_k) {
+      const int r = (i * 256 + tid) / PARTS;
       float dot = 0.f;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) dot = fmaf(val[i][e], mean[e], dot);
+      for (int e = 0; e < 8; ++e) dot = fmaf(val[e], mean[e], dot);
 #pragma unroll
       for (int o = PARTS / 2; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
       if (part == 0 && blk * 128 + r < N) lse_corr[row0 + r] = scale * dot;
@@ -151,12 +157,19 @@ __global__ void __launch_bounds__(256, 2) fa_quant_kernel(
   for (int w = 1; w < 8; ++w) amax = fmaxf(amax, wmax[w]);
   const float s = amax > 0.f ? amax / kE4M3Max : 1.f;
   const float inv = 1.f / s;
+  // Convert again from bf16 below rather than keep the first pass's fp32
+  // values live across the barrier (that would double the registers).
+#pragma unroll
+  for (int i = 0; i < PER; ++i)
+    asm volatile("" : "+r"(raw[i].x), "+r"(raw[i].y), "+r"(raw[i].z), "+r"(raw[i].w));
   if (tid == 0) (is_k ? k_scale : q_scale)[(size_t)bh * nblk + blk] = s;
   uint2* dst = reinterpret_cast<uint2*>((is_k ? k8 : q8) + row0 * D);
 #pragma unroll
   for (int i = 0; i < PER; ++i) {
     const int chunk = i * 256 + tid;
     if (blk * 128 + chunk / PARTS >= N) continue;
+    float val[8];
+    values(i, val);
     uint32_t w[2];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
@@ -165,7 +178,7 @@ __global__ void __launch_bounds__(256, 2) fa_quant_kernel(
 #pragma unroll
       for (int b = 0; b < 4; ++b) {
         const __nv_fp8_storage_t v8 =
-            __nv_cvt_float_to_fp8(val[i][4 * h + b] * inv, __NV_SATFINITE, __NV_E4M3);
+            __nv_cvt_float_to_fp8(val[4 * h + b] * inv, __NV_SATFINITE, __NV_E4M3);
         word |= (uint32_t)v8 << (8 * b);
       }
       w[h] = word;
