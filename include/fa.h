@@ -109,6 +109,11 @@ typedef struct fa_mask {
  *
  *   mask  NULL or kind FA_MASK_NONE: no mask; otherwise as fa_mask above.  An
  *         ADDITIVE mask must be 4-byte aligned; a mask must not overlap out or lse.
+ *         Speed, not results, depends on alignment: an ADDITIVE mask whose rows
+ *         start 16-byte aligned (16-byte aligned data, Nk a multiple of 4) is
+ *         copied tile by tile into shared memory by TMA; a BOOL mask with
+ *         16-byte aligned rows is read 16 bytes at a time; other masks are
+ *         read element by element.
  *   other arguments as fa_fwd.
  *
  * Rows left with no key give O = 0, LSE = -inf.  Errors as fa_fwd, plus

@@ -186,3 +186,19 @@ def test_staged_mask_many_units(D, kind, per_head):
     out, lse = _run(inp, full_mask=m.contiguous())
     o_ref, l_ref = _oracle(inp, full_mask=ref, rows=rows)
     compare(out, lse, o_ref, l_ref, rows=rows, label=f"staged {kind} D{D} heads {mh}")
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("Nq,Nk", [(600, 1040), (1000, 400), (300, 900)])
+def test_staged_additive_mask_with_causal(D, Nq, Nk):
+    """A staged fp32 mask with the causal triangle: causal units stop at their
+    last query row's key block, and the mask copier must walk the same
+    shortened key ranges (Nq > Nk and Nq < Nk both)."""
+    B, H = 2, 3
+    inp = _inputs(D, B, H, Nq, Nk)
+    g = torch.Generator(device="cuda").manual_seed(31)
+    m = torch.randn(B, H, Nq, Nk, generator=g, device="cuda") * 1.5
+    m[1, :, :, ::7] = float("-inf")
+    out, lse = _run(inp, full_mask=m.contiguous(), causal=True)
+    o_ref, l_ref = _oracle(inp, full_mask=m, causal=True)
+    compare(out, lse, o_ref, l_ref, label=f"staged causal D{D} {Nq}x{Nk}")
