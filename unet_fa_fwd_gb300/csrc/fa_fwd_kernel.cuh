@@ -15,11 +15,15 @@
 //   warps 4-7  softmax warpgroup for query tile 1
 //   warp  8    TMA producer: Q tiles, then K_j, V_j into a shared-memory ring
 //   warp  9    MMA issuer and TMEM owner (the warp runs the loop, one elected
-//              lane issues each MMA batch and commit)
-//   warps 10-11 idle
+//              lane issues each MMA batch and commit); at D <= 64 tile 0's
+//              MMAs only
+//   warp  10   staged fp32 mask: the mask copier (TMA); otherwise idle
+//   warp  11   D <= 64: tile 1's MMA issuer; otherwise idle
 // Tensor memory (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+D),
-// O1 [256+D, 256+2D).  P (bf16) is written over the first 64 columns of its
-// S block and fed to the P·V MMA straight from tensor memory.
+// O1 [256+D, 256+2D).  At D = 128 P (bf16) is written over the first 64
+// columns of its S block; at D <= 64 P0 and P1 have 64 columns of their own
+// after O1, so the next S can be computed while P waits for its P·V.  P is
+// fed to the P·V MMA straight from tensor memory.
 //
 // Every mbarrier wait is bounded in time: past the limit the CTA records
 // FA_ERR_TIMEOUT in a device status word, drains its own in-flight copies and
@@ -160,9 +164,9 @@ struct Cfg {
   static_assert(!SEP_P || COL_P1 + 64 <= TMEM_COLS, "tensor-memory columns");
   static constexpr int THREADS = 384;
   // Launch: 168 registers x 384 threads.  The softmax warpgroups (0, 1)
-  // rise to REGS_SOFTMAX, warpgroup 2 (producer, MMA, idle) drops to
-  // REGS_OTHER; the sum stays within 384*168, so the increase never waits on
-  // registers that do not exist.
+  // rise to REGS_SOFTMAX, warpgroup 2 (producer, MMA, copier or second MMA)
+  // drops to REGS_OTHER; the sum stays within 384*168, so the increase never
+  // waits on registers that do not exist.
 #ifndef FA_REGS_SOFTMAX
 #define FA_REGS_SOFTMAX 184
 #define FA_REGS_OTHER 136
@@ -825,11 +829,12 @@ __global__ void __launch_bounds__(Cfg<D, F8, MK>::THREADS, 1)
             ptx::mma_ss_x2_el<C::s_off(1)>(d, a, dq_hi, b, dk_hi, IDESC_QK, 0);
         }
       };
-      // O_t += P_t V : A = P (tensor memory, over the S_t block), B = V tile
-      // (MN-major: the head dim is contiguous), K-dim = 128 keys in 8 MMAs,
-      // issued as two batches of 64 keys: the softmax releases P in halves.
-      // A half of P is 32 tensor-memory columns (bf16 pairs); 64 keys of V
-      // are 64 rows of the V tile.
+      // O_t += P_t V : A = P (tensor memory: over the S_t block at D = 128,
+      // its own columns at D <= 64), B = V tile (MN-major: the head dim is
+      // contiguous), K-dim = 128 keys in 8 MMAs; at D = 128 issued as two
+      // batches of 64 keys (the softmax releases P in halves), at D <= 64 as
+      // one.  A half of P is 32 tensor-memory columns (bf16 pairs); 64 keys of
+      // V are 64 rows of the V tile.
       constexpr uint32_t kVStep16 = (16 * C::SW) >> 4;
       auto issue_pv_half = [&](int t, uint32_t stg, int half, bool first) {
         const uint32_t b = dv_lo + stg * kTile16 + half * 4 * kVStep16;
