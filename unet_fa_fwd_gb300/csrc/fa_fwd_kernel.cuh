@@ -257,8 +257,8 @@ __device__ __forceinline__ Unit decode_unit(const Params& p, int u) {
   } else if (p.causal) {
     // Causal (one key range): a pair's work grows with its query position, so
     // units run heaviest first across all heads (pair index descending, heads
-    // inner); with the round-robin assignment this keeps the CTAs' totals
-    // within a few percent, and the units of a head still start together.
+    // inner); dealt to the CTAs in snake order (snake_unit) this keeps the
+    // CTAs' totals close, and the units of a head still start together.
     const uint32_t k = p.div_bh.div((uint32_t)u);
     r.split = 0;
     r.bh = u - (int)k * p.BH;
@@ -289,6 +289,18 @@ __device__ __forceinline__ Unit decode_unit(const Params& p, int u) {
     r.ntiles = min(r.ntiles, last_row / 128 + 1 - r.tile0);
   }
   return r;
+}
+
+// The CTA's ui-th unit.  Units are dealt to the persistent CTAs round by
+// round, in ascending CTA order in even rounds and descending order in odd
+// ones (a snake): with units sorted heaviest first (causal launches) each
+// CTA's total stays near the mean, where a plain round-robin gives CTA 0 the
+// heaviest unit of every round; a round's set of units (what runs together,
+// sharing L2) is unchanged.  Past INT_MAX the index saturates (>= num_units).
+__device__ __forceinline__ int snake_unit(int ui) {
+  const long long G = gridDim.x, c = blockIdx.x;
+  const long long v = (long long)ui * G + ((ui & 1) ? G - 1 - c : c);
+  return v > INT_MAX ? INT_MAX : (int)v;
 }
 
 // Host side of the unit schedule, last-wave balancing: with P pair units on
@@ -706,7 +718,7 @@ __global__ void __launch_bounds__(Cfg<D, F8, MK>::THREADS, 1)
       uint32_t skipped = 0xffffffffu;  // the tile the stall hook withheld, if any
       uint32_t q_issued = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uc) {
+      for (int ui = 0, u = snake_unit(0); u < p.num_units && ok; u = snake_unit(++ui), ++uc) {
         const Unit un = decode_unit(p, u);
         const int bh = un.bh, q0 = un.q0;
         const int ntiles = un.nq;
@@ -915,7 +927,7 @@ __global__ void __launch_bounds__(Cfg<D, F8, MK>::THREADS, 1)
           ptx::mma_commit_el(ptx::smem_u32(&bars->s_full[mt]));
           return true;
         };
-        for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uc) {
+        for (int ui = 0, u = snake_unit(0); u < p.num_units && ok; u = snake_unit(++ui), ++uc) {
           const Unit un = decode_unit(p, u);
           const bool mine = mt == 0 || un.nq == 2;
           const int nkv = un.ntiles;
@@ -957,7 +969,7 @@ __global__ void __launch_bounds__(Cfg<D, F8, MK>::THREADS, 1)
           }
         }
       } else {
-        for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uc) {
+        for (int ui = 0, u = snake_unit(0); u < p.num_units && ok; u = snake_unit(++ui), ++uc) {
           const Unit un = decode_unit(p, u);
           const bool has1 = un.nq == 2;
           const int nkv = un.ntiles;
@@ -1038,7 +1050,7 @@ __global__ void __launch_bounds__(Cfg<D, F8, MK>::THREADS, 1)
         ptx::tma_prefetch_desc(&p.tm_mask);
         uint32_t mc = 0;  // pieces issued
         bool ok = true;
-        for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+        for (int ui = 0, u = snake_unit(0); u < p.num_units && ok; u = snake_unit(++ui)) {
           const Unit un = decode_unit(p, u);
           if (!fa_check(p, bars, unit_in_bounds(p, un), kCheckUnit, u, un.bh)) {
             ok = false;
@@ -1121,7 +1133,7 @@ __global__ void __launch_bounds__(Cfg<D, F8, MK>::THREADS, 1)
     uint32_t mpiece = 0;  // staged masks: pieces of the units before this one
     bool ok = true;
 
-    for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+    for (int ui = 0, u = snake_unit(0); u < p.num_units && ok; u = snake_unit(++ui)) {
       const Unit un = decode_unit(p, u);
       const int bh = un.bh, q0 = un.q0;
       const uint32_t unit_piece0 = mpiece;
