@@ -553,6 +553,9 @@ __device__ __forceinline__ float general_pass1(uint32_t tS, const void* mrow, in
 __device__ __forceinline__ float general_pass1_key4(uint32_t tS, float4 kv, int lo, uint32_t span,
                                                     float sl2, int nsteps) {
   constexpr float kLog2e = 1.4426950408889634f;
+  const float2 sl22 = make_float2(sl2, sl2), l2e2 = make_float2(kLog2e, kLog2e);
+  // Every row of the warp keeps every key of the block: no key-range selects.
+  const bool full = __all_sync(0xffffffffu, lo == 0 && span >= 128u);
   float mx = -INFINITY;
   const int end = nsteps * kGenStep;  // nsteps is even: 32 keys per iteration
 #pragma unroll 1
@@ -566,12 +569,18 @@ __device__ __forceinline__ float general_pass1_key4(uint32_t tS, float4 kv, int 
       const float mv[4] = {__shfl_sync(0xffffffffu, kv.x, src), __shfl_sync(0xffffffffu, kv.y, src),
                            __shfl_sync(0xffffffffu, kv.z, src), __shfl_sync(0xffffffffu, kv.w, src)};
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
+      for (int e = 0; e < 4; e += 2) {  // f32x2 pairs
         const int i = 4 * q + e;
-        float t = fmaf(mv[e], kLog2e, __uint_as_float(r[i]) * sl2);
-        t = (uint32_t)(d + i) < span ? t : -INFINITY;
-        mx = fmaxf(mx, t);
-        r[i] = __float_as_uint(t);
+        float2 t = __ffma2_rn(make_float2(mv[e], mv[e + 1]), l2e2,
+                              __fmul2_rn(make_float2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])),
+                                         sl22));
+        if (!full) {
+          t.x = (uint32_t)(d + i) < span ? t.x : -INFINITY;
+          t.y = (uint32_t)(d + i + 1) < span ? t.y : -INFINITY;
+        }
+        mx = ptx::fmax3(mx, t.x, t.y);
+        r[i] = __float_as_uint(t.x);
+        r[i + 1] = __float_as_uint(t.y);
       }
     }
     ptx::tmem_st32x32b_x32(tS + cb, r);
@@ -601,6 +610,10 @@ __device__ __forceinline__ float general_pass1_staged(uint32_t tS, const uint8_t
   constexpr int STEPS = PK / kGenStep;      // 16-key steps per piece
   const uint32_t lane = threadIdx.x & 31;
   const int rsw = row & 7;
+  const float2 sl22 = make_float2(sl2, sl2), l2e2 = make_float2(kLog2e, kLog2e);
+  // Every row of the warp keeps every key of the block (no Nk tail, causal
+  // diagonal or segment boundary in it): no key-range selects.
+  const bool full = __all_sync(0xffffffffu, lo == 0 && span >= 128u);
   float mx = -INFINITY;
 #pragma unroll 1
   for (int pc = 0; pc < NP; ++pc) {
@@ -625,12 +638,20 @@ __device__ __forceinline__ float general_pass1_staged(uint32_t tS, const uint8_t
       uint32_t r[kGenStep];
       ptx::tmem_ld32x32b_x16(tS + cb, r);
       const int d = cb - lo;
+      // Scores and mask values in f32x2 pairs; the key-range selects only
+      // where some row of the warp does not keep the whole block.
 #pragma unroll
-      for (int i = 0; i < kGenStep; ++i) {
-        float t = fmaf(__uint_as_float(w[i]), kLog2e, __uint_as_float(r[i]) * sl2);
-        t = (uint32_t)(d + i) < span ? t : -INFINITY;
-        mx = fmaxf(mx, t);
-        r[i] = __float_as_uint(t);
+      for (int i = 0; i < kGenStep; i += 2) {
+        float2 t = __ffma2_rn(make_float2(__uint_as_float(w[i]), __uint_as_float(w[i + 1])), l2e2,
+                              __fmul2_rn(make_float2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])),
+                                         sl22));
+        if (!full) {
+          t.x = (uint32_t)(d + i) < span ? t.x : -INFINITY;
+          t.y = (uint32_t)(d + i + 1) < span ? t.y : -INFINITY;
+        }
+        mx = ptx::fmax3(mx, t.x, t.y);
+        r[i] = __float_as_uint(t.x);
+        r[i + 1] = __float_as_uint(t.y);
       }
       ptx::tmem_st32x32b_x16(tS + cb, r);
     }
@@ -1360,10 +1381,13 @@ __global__ void __launch_bounds__(Cfg<D, F8, MK>::THREADS, 1)
             if (cb < nsteps * kGenStep) {
               uint32_t r[32];
               ptx::tmem_ld32x32b_x32(tS + cb, r);
+              const float2 nm2 = make_float2(-m_use, -m_use);
 #pragma unroll
               for (int c = 0; c < 32; c += 2) {
-                const float p0 = ptx::ex2(__uint_as_float(r[c]) - m_use);
-                const float p1 = ptx::ex2(__uint_as_float(r[c + 1]) - m_use);
+                const float2 x =
+                    __fadd2_rn(make_float2(__uint_as_float(r[c]), __uint_as_float(r[c + 1])), nm2);
+                const float p0 = ptx::ex2(x.x);
+                const float p1 = ptx::ex2(x.y);
                 lsum = __fadd2_rn(lsum, make_float2(p0, p1));
                 packed[c / 2] = ptx::pack_bf16x2(p0, p1);
               }
