@@ -607,7 +607,6 @@ __device__ __forceinline__ float general_pass1_staged(uint32_t tS, const uint8_t
   constexpr int PK = 32;                    // keys per piece
   constexpr int NP = 128 / PK;              // pieces per block
   constexpr int PB = 128 * 128;             // bytes per piece
-  constexpr int STEPS = PK / kGenStep;      // 16-key steps per piece
   const uint32_t lane = threadIdx.x & 31;
   const int rsw = row & 7;
   const float2 sl22 = make_float2(sl2, sl2), l2e2 = make_float2(kLog2e, kLog2e);
@@ -624,36 +623,34 @@ __device__ __forceinline__ float general_pass1_staged(uint32_t tS, const uint8_t
       return mx;
     }
     const uint8_t* rowp = sMask + (idx % kMaskSlots) * PB + row * 128;
-#pragma unroll 1
-    for (int st = 0; st < STEPS; ++st) {
-      const int cb = pc * PK + st * kGenStep;
-      if (cb >= nsteps * kGenStep) break;
-      uint32_t w[kGenStep];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int c = st * 4 + i;  // 16-byte chunk of the 128-byte row
-        const uint4 v = *reinterpret_cast<const uint4*>(rowp + ((c ^ rsw) << 4));
-        w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
-      }
-      uint32_t r[kGenStep];
-      ptx::tmem_ld32x32b_x16(tS + cb, r);
+    const int cb = pc * PK;  // the piece's 32 keys in one tensor-memory round trip
+    if (cb < nsteps * kGenStep) {
+      uint32_t r[PK];
+      ptx::tmem_ld32x32b_x32(tS + cb, r);
       const int d = cb - lo;
       // Scores and mask values in f32x2 pairs; the key-range selects only
       // where some row of the warp does not keep the whole block.
 #pragma unroll
-      for (int i = 0; i < kGenStep; i += 2) {
-        float2 t = __ffma2_rn(make_float2(__uint_as_float(w[i]), __uint_as_float(w[i + 1])), l2e2,
-                              __fmul2_rn(make_float2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])),
-                                         sl22));
-        if (!full) {
-          t.x = (uint32_t)(d + i) < span ? t.x : -INFINITY;
-          t.y = (uint32_t)(d + i + 1) < span ? t.y : -INFINITY;
+      for (int ch = 0; ch < 8; ++ch) {  // 16-byte chunks of the row's 128 bytes
+        const uint4 v = *reinterpret_cast<const uint4*>(rowp + ((ch ^ rsw) << 4));
+        const float w[4] = {__uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z),
+                            __uint_as_float(v.w)};
+#pragma unroll
+        for (int e = 0; e < 4; e += 2) {
+          const int i = 4 * ch + e;
+          float2 t = __ffma2_rn(make_float2(w[e], w[e + 1]), l2e2,
+                                __fmul2_rn(make_float2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])),
+                                           sl22));
+          if (!full) {
+            t.x = (uint32_t)(d + i) < span ? t.x : -INFINITY;
+            t.y = (uint32_t)(d + i + 1) < span ? t.y : -INFINITY;
+          }
+          mx = ptx::fmax3(mx, t.x, t.y);
+          r[i] = __float_as_uint(t.x);
+          r[i + 1] = __float_as_uint(t.y);
         }
-        mx = ptx::fmax3(mx, t.x, t.y);
-        r[i] = __float_as_uint(t.x);
-        r[i + 1] = __float_as_uint(t.y);
       }
-      ptx::tmem_st32x32b_x16(tS + cb, r);
+      ptx::tmem_st32x32b_x32(tS + cb, r);
     }
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->m_empty[idx % kMaskSlots]));
