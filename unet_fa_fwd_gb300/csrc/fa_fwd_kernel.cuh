@@ -1372,28 +1372,40 @@ __global__ void __launch_bounds__(Cfg<D, F8, MK>::THREADS, 1)
           // (at D = 128 the first 64 columns of S, behind the columns still to
           // be read).  Columns past the steps pass 1 processed are excluded
           // for every row: P = 0 there.
-#pragma unroll 1
-          for (int cb = 0; cb < 128; cb += 32) {
-            uint32_t packed[16];
-            if (cb < nsteps * kGenStep) {
-              uint32_t r[32];
-              ptx::tmem_ld32x32b_x32(tS + cb, r);
-              const float2 nm2 = make_float2(-m_use, -m_use);
+          // 64 columns per tensor-memory round trip where all of them hold
+          // values, else 32 (pass 1 processed a multiple of 32 columns).
+          const int end = nsteps * kGenStep;
+          const float2 nm2 = make_float2(-m_use, -m_use);
+          auto exps = [&](const uint32_t* r, uint32_t* packed, int n) {
 #pragma unroll
-              for (int c = 0; c < 32; c += 2) {
-                const float2 x =
-                    __fadd2_rn(make_float2(__uint_as_float(r[c]), __uint_as_float(r[c + 1])), nm2);
-                const float p0 = ptx::ex2(x.x);
-                const float p1 = ptx::ex2(x.y);
-                lsum = __fadd2_rn(lsum, make_float2(p0, p1));
-                packed[c / 2] = ptx::pack_bf16x2(p0, p1);
-              }
+            for (int c = 0; c < 64; c += 2) {
+              if (c >= n) break;
+              const float2 x =
+                  __fadd2_rn(make_float2(__uint_as_float(r[c]), __uint_as_float(r[c + 1])), nm2);
+              const float p0 = ptx::ex2(x.x);
+              const float p1 = ptx::ex2(x.y);
+              lsum = __fadd2_rn(lsum, make_float2(p0, p1));
+              packed[c / 2] = ptx::pack_bf16x2(p0, p1);
+            }
+          };
+#pragma unroll 1
+          for (int cb = 0; cb < 128; cb += 64) {
+            uint32_t packed[32];
+            if (cb + 64 <= end) {
+              uint32_t r[64];
+              ptx::tmem_ld32x32b_x64(tS + cb, r);
+              exps(r, packed, 64);
             } else {
 #pragma unroll
-              for (int c = 0; c < 16; ++c) packed[c] = 0u;
+              for (int c = 0; c < 32; ++c) packed[c] = 0u;
+              if (cb < end) {
+                uint32_t r[32];
+                ptx::tmem_ld32x32b_x32(tS + cb, r);
+                exps(r, packed, 32);
+              }
             }
-            ptx::tmem_st32x32b_x16(tP + cb / 2, packed);
-            if (!C::SEP_P && cb == 32 && !rescale_o) release(0);
+            ptx::tmem_st32x32b_x32(tP + cb / 2, packed);
+            if (!C::SEP_P && cb == 0 && !rescale_o) release(0);
           }
           free_s();
         }
