@@ -510,9 +510,8 @@ __device__ __forceinline__ float general_pass1(uint32_t tS, const void* mrow, in
                                                uint32_t (&a)[kGenStep], uint32_t (&b)[kGenStep]) {
   constexpr float kLog2e = 1.4426950408889634f;
   float mx = -INFINITY;
-  auto step = [&](int cb, uint32_t (&w)[kGenStep]) {
-    uint32_t r[kGenStep];
-    ptx::tmem_ld32x32b_x16(tS + cb, r);
+  // 16 scores of r (starting at column cb) with the mask values w.
+  auto step = [&](int cb, uint32_t* r, const uint32_t (&w)[kGenStep]) {
     const int d = cb - lo;
 #pragma unroll
     for (int i = 0; i < kGenStep; ++i) {
@@ -527,19 +526,22 @@ __device__ __forceinline__ float general_pass1(uint32_t tS, const void* mrow, in
       mx = fmaxf(mx, t);
       r[i] = __float_as_uint(t);
     }
-    ptx::tmem_st32x32b_x16(tS + cb, r);
   };
   const int end = nsteps * kGenStep;
 #pragma unroll 1
   for (int cb = 0; cb < end; cb += 2 * kGenStep) {
-    // Each buffer is refilled as soon as its step has used it, with the keys
-    // it serves two steps later (clamped to the block: the last pair reloads
-    // its own keys, which are never used).
+    // One tensor-memory round trip per pair of steps.  Each buffer is
+    // refilled as soon as its step has used it, with the keys it serves two
+    // steps later (clamped to the block: the last pair reloads its own keys,
+    // which are never used).
     const int nb = kbase + min(cb + 2 * kGenStep, 128 - 2 * kGenStep);
-    step(cb, a);
+    uint32_t r[2 * kGenStep];
+    ptx::tmem_ld32x32b_x32(tS + cb, r);
+    step(cb, r, a);
     general_load<MK>(mrow, nb, Nk, a);
-    step(cb + kGenStep, b);
+    step(cb + kGenStep, r + kGenStep, b);
     general_load<MK>(mrow, nb + kGenStep, Nk, b);
+    ptx::tmem_st32x32b_x32(tS + cb, r);
   }
   return mx;
 }
