@@ -423,9 +423,11 @@ __device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity, Barr
   }
 }
 
-// Warp-uniform version: every lane waits, then the warp agrees.
+// Warp-uniform version: every lane waits, then the warp agrees.  A phase
+// that has already completed is taken with one test and one vote.
 __device__ __forceinline__ bool bounded_wait_warp(uint32_t bar, uint32_t parity, Barriers* bars,
                                                   unsigned long long timeout_ns, int* status) {
+  if (__all_sync(0xffffffffu, ptx::mbar_try_wait(bar, parity))) return true;
   bool ok = bounded_wait(bar, parity, bars, timeout_ns, status);
   return __all_sync(0xffffffffu, ok);
 }
