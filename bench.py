@@ -147,6 +147,32 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- distributed
 
+def launches_per_step(step, device) -> int:
+    """Kernels of this library one call of `step` launches, counted from the
+    library's own launch log (FA_LOG=1 describes every launch on stderr; the
+    descriptor is redirected to a temporary file for the one call)."""
+    import re
+    import tempfile
+    import torch
+    torch.cuda.synchronize(device)
+    sys.stderr.flush()
+    saved = os.dup(2)
+    with tempfile.TemporaryFile() as f:
+        os.dup2(f.fileno(), 2)
+        os.environ["FA_LOG"] = "1"
+        try:
+            step()
+            torch.cuda.synchronize(device)
+        finally:
+            os.environ.pop("FA_LOG", None)
+            os.dup2(saved, 2)
+            os.close(saved)
+        f.seek(0)
+        text = f.read().decode(errors="replace")
+    return sum(len(re.findall(r"\bfa_\w+_kernel\b", ln))
+               for ln in text.splitlines() if ln.startswith("[fa] "))
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -291,6 +317,7 @@ def bench_native(args, world, rank, local):
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(device)
+    kernels_per_step = launches_per_step(step, device)
     if fa.read_device_status(stream) != 0:
         raise RuntimeError("kernel wait timed out during warm-up")
 
@@ -529,8 +556,8 @@ def bench_native(args, world, rank, local):
             win[f"{wh}x{wwid}_shift{sh}"] = {"ms_per_step": round(msw, 4),
                                             "tflops": round(wfl / msw / 1e9, 1)}
         ext["window"] = {"workload": "sd_self grid 64x64, B2 H8 D64",
-                         "note": "gather + attention + scatter kernels, outputs allocated by the "
-                                 "binding", "configs": win}
+                         "note": "one attention launch that gathers and scatters the window "
+                                 "rows itself; outputs allocated by the binding", "configs": win}
         del ww
         # causal at the benchmark shape: the useful FLOPs count keys j <= i only
         oc_, lc_ = torch.empty_like(q), torch.empty_like(lse)
@@ -651,7 +678,7 @@ def bench_native(args, world, rank, local):
                      "overlap": "double-buffered: upload i+1 (Q on one copy stream, K/V on "
                                 "another) / download i-1 overlap kernel i"}
                     if e2e_steps else None),
-            "gpu_launches": args.steps,
+            "gpu_launches": kernels_per_step * args.steps,
             "roofline": {"bound": "tensor", "achieved": round(kernel_tflops, 2), "peak": peak,
                          "unit": "TFLOP/s", "frac": round(kernel_tflops / peak, 4),
                          "traffic": read_traffic(args.workload),

@@ -200,28 +200,30 @@ FA_API int fa_split_count(int B, int H, int Nq, int Nk, int num_sms);
  * grid: every token attends only to the tokens of its own win_h x win_w window
  * of the grid cyclically shifted by (shift_h, shift_w) (the token at (r, c)
  * moves to ((r - shift_h) mod img_h, (c - shift_w) mod img_w)).  Computed as in
- * "Step 3.7 Flash" §3.2: the windows are gathered into a batch of
- * B * (img_h/win_h) * (img_w/win_w) attention problems of win_h*win_w tokens,
- * run through fa_fwd, and O / LSE are scattered back to token order.  No mask
- * is applied across the wrap-around of a shifted grid (the pages name none).
+ * "Step 3.7 Flash" §3.2: the windows form a batch of
+ * B * (img_h/win_h) * (img_w/win_w) attention problems of win_h*win_w tokens.
+ * Here the batch is never materialised: the attention kernel reads each
+ * window's rows of q, k, v from their grid positions and writes O and LSE
+ * back to them.  Windows of up to 64 tokens are packed several to a batch
+ * entry, each row seeing only its own window's keys.  No mask is applied
+ * across the wrap-around of a shifted grid (the pages name none).
  *
  *   q, k, v, out  device bf16 [B, H, img_h*img_w, D], tokens in row-major grid order
  *   lse           device fp32 [B, H, img_h*img_w]
  *   win_h, win_w  >= 1 and dividing img_h, img_w;  shift_h, shift_w any integers
- *   workspace     device scratch, 16-byte aligned, at least
- *                 fa_window_workspace_bytes(B, H, img_h, img_w, D) bytes, owned by
- *                 the caller and not shared with a concurrent call
+ *   workspace,    not used (fa_window_workspace_bytes returns 0); any value,
+ *   workspace_bytes  NULL and 0 included, is accepted
  *   other arguments as fa_fwd
  *
- * Three kernels (gather, attention, scatter) are enqueued on `stream`.
- * Errors as fa_fwd, plus FA_ERR_INVALID_ARGUMENT for windows that do not tile
- * the grid or a missing, misaligned, small or overlapping workspace.
+ * One kernel is enqueued on `stream`.  Errors as fa_fwd, plus
+ * FA_ERR_INVALID_ARGUMENT for windows that do not tile the grid or more than
+ * 2^31 - 1 rows (B * H * img_h * img_w).
  */
 FA_API int fa_fwd_window(const void* q, const void* k, const void* v, void* out, float* lse, int B, int H,
                   int img_h, int img_w, int D, int win_h, int win_w, int shift_h, int shift_w,
                   float scale, void* workspace, size_t workspace_bytes, void* stream);
 
-/* Workspace bytes fa_fwd_window needs (0 for invalid sizes). */
+/* Workspace bytes fa_fwd_window needs: 0 (kept for callers that size one). */
 FA_API size_t fa_window_workspace_bytes(int B, int H, int img_h, int img_w, int D);
 
 /* Bytes of the fixed device scratch that fa_fwd_split_noalloc uses. */

@@ -5,6 +5,7 @@ import os
 import re
 
 import pytest
+import torch
 
 import unet_fa_fwd_gb300 as fa
 from unet_fa_fwd_gb300 import _build
@@ -146,19 +147,23 @@ def test_fa_fwd_ex_mask_validation_before_any_cuda_call(lib):
 
 def test_window_validation_before_any_cuda_call(lib):
     raw = fa.load_library()
-    assert fa.window_workspace_bytes(1, 2, 8, 8, 64) == 4 * (2 * 64 * 64 * 2) + 2 * 64 * 4
+    # the attention kernel gathers and scatters window rows itself: no workspace
+    assert fa.window_workspace_bytes(1, 2, 8, 8, 64) == 0
     assert fa.window_workspace_bytes(0, 2, 8, 8, 64) == 0
 
-    def call(img=(8, 8), win=(4, 4), D=64, ws=0xA0000, ws_bytes=1 << 20, q=0x10000):
-        return raw.fa_fwd_window(q, 0x20000, 0x30000, 0x40000, 0x50000, 1, 2, img[0], img[1], D,
+    def call(img=(8, 8), win=(4, 4), D=64, ws=None, ws_bytes=0, q=0x10000, B=1, out=0x40000):
+        return raw.fa_fwd_window(q, 0x20000, 0x30000, out, 0x50000, B, 2, img[0], img[1], D,
                                  win[0], win[1], 1, 1, ctypes.c_float(0.1), ws, ws_bytes, None)
     assert call(win=(3, 4)) == 1       # windows must tile the grid
     assert call(win=(0, 4)) == 1
     assert call(D=48) == 2
-    assert call(ws=None) == 1
-    assert call(ws=0xA0008) == 1       # misaligned workspace
-    assert call(ws_bytes=100) == 1
     assert call(q=None) == 1
+    assert call(q=0x10008) == 1        # misaligned tensor
+    assert call(out=0x10000) == 1      # O overlaps Q
+    assert call(B=1 << 20, img=(64, 64), win=(8, 8)) == 1   # 2^31 rows or more
+    if not torch.cuda.is_available():
+        # valid arguments (any workspace): the first CUDA call fails on this machine
+        assert call() == 3 and call(ws=0xA0000, ws_bytes=1 << 20) == 3
 
 
 def test_fp8_validation_before_any_cuda_call(lib):

@@ -59,3 +59,19 @@ def test_window_validation():
     inp = workloads.make_inputs("sd_self", device="cuda", B=1, H=1, Nq=64, Nk=64)
     with pytest.raises(RuntimeError, match="INVALID_ARGUMENT"):
         fa.fwd_window(inp["q"], inp["k"], inp["v"], 8, 8, 3, 3)    # 3 does not divide 8
+
+
+
+def test_window_is_one_launch_without_workspace(monkeypatch, capfd):
+    """The windows are gathered and scattered by the attention kernel itself:
+    one launch, no workspace (fa_window_workspace_bytes is 0)."""
+    inp = workloads.make_inputs("sd_self", device="cuda", B=1, H=2)
+    assert fa.window_workspace_bytes(1, 2, 64, 64, 64) == 0
+    capfd.readouterr()
+    monkeypatch.setenv("FA_LOG", "1")
+    out, lse = fa.fwd_window(inp["q"], inp["k"], inp["v"], 64, 64, 8, 8, 4, 4, scale=inp["scale"])
+    torch.cuda.synchronize()
+    monkeypatch.delenv("FA_LOG")
+    assert fa.read_device_status() == 0
+    kernels = [ln for ln in capfd.readouterr().err.splitlines() if ln.startswith("[fa] fa_")]
+    assert len(kernels) == 1 and "window rows" in kernels[0], kernels

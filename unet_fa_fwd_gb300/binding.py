@@ -267,20 +267,21 @@ def fwd_window(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, img_h: int, im
                win_h: int, win_w: int, shift_h: int = 0, shift_w: int = 0,
                scale: float | None = None, stream=None):
     """Window / shifted-window attention; q, k, v bf16 [B, H, img_h*img_w, D] in grid order.
-    Allocates outputs and the workspace with torch; returns (O, LSE)."""
+    Allocates the outputs with torch (no workspace is needed); returns (O, LSE)."""
     B, H, N, D = q.shape
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _check(t, n, torch.bfloat16, (B, H, N, D))
     out = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
-    ws = torch.empty(max(16, window_workspace_bytes(B, H, img_h, img_w, D)), dtype=torch.uint8,
-                     device=q.device)
+    ws_bytes = window_workspace_bytes(B, H, img_h, img_w, D)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device) if ws_bytes else None
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     rc = load_library().fa_fwd_window(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                                        lse.data_ptr(), B, H, img_h, img_w, D, win_h, win_w,
-                                       shift_h, shift_w, ctypes.c_float(scale), ws.data_ptr(),
-                                       ws.numel(), _stream_handle(stream))
+                                       shift_h, shift_w, ctypes.c_float(scale),
+                                       None if ws is None else ws.data_ptr(), ws_bytes,
+                                       _stream_handle(stream))
     if rc != FA_OK:
         raise RuntimeError(f"fa_fwd_window failed: {status_string(rc)}")
     return out, lse

@@ -14,7 +14,7 @@ namespace fa {
 
 constexpr int kLaunchMaxDevices = 64;
 
-template <int D, bool F8, int MK>
+template <int D, bool F8, int MK, bool WIN = false>
 int launch_one(const Params& prm, int device, int sm_count, cudaStream_t stream) {
   using C = Cfg<D, F8, MK>;
   static std::mutex mu;
@@ -23,14 +23,14 @@ int launch_one(const Params& prm, int device, int sm_count, cudaStream_t stream)
   {
     std::lock_guard<std::mutex> lock(mu);
     if (!ready[device]) {
-      if (cudaFuncSetAttribute(fa_fwd_kernel<D, F8, MK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      if (cudaFuncSetAttribute(fa_fwd_kernel<D, F8, MK, WIN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                C::SMEM_BYTES) != cudaSuccess)
         return FA_ERR_CUDA;
       // The warpgroup register split (setmaxnreg) must fit in the registers
       // the launch reserves, or the increase would wait forever: refuse to
       // launch a build where it does not.
       cudaFuncAttributes fattr;
-      if (cudaFuncGetAttributes(&fattr, fa_fwd_kernel<D, F8, MK>) != cudaSuccess) return FA_ERR_CUDA;
+      if (cudaFuncGetAttributes(&fattr, fa_fwd_kernel<D, F8, MK, WIN>) != cudaSuccess) return FA_ERR_CUDA;
       if (2 * 128 * C::REGS_SOFTMAX + 128 * C::REGS_OTHER > fattr.numRegs * C::THREADS)
         return FA_ERR_UNSUPPORTED;
       ready[device] = true;
@@ -39,16 +39,16 @@ int launch_one(const Params& prm, int device, int sm_count, cudaStream_t stream)
   const int grid = prm.num_units < sm_count ? prm.num_units : sm_count;
   static const char* kMaskNames[] = {"none", "key fp32x4", "fp32", "u8x16", "u8",
                                       "fp32 staged"};
-  log_launch("fa_fwd_kernel<D=%d,%s,mask %s> tile %dx%d grid %d x %d threads smem %d B tmem %d cols "
+  log_launch("fa_fwd_kernel<D=%d,%s,mask %s%s> tile %dx%d grid %d x %d threads smem %d B tmem %d cols "
              "stages %d units %d (single-tile from %d) key ranges %d BH %d Nq %d Nk %d "
              "mask %s causal %d seg %d",
-             D, F8 ? "e4m3 QK" : "bf16", kMaskNames[MK], C::BM, C::BN, grid, C::THREADS,
+             D, F8 ? "e4m3 QK" : "bf16", kMaskNames[MK], WIN ? ",window rows" : "", C::BM, C::BN, grid, C::THREADS,
              C::SMEM_BYTES, C::TMEM_COLS, C::STAGES, prm.num_units, prm.tail_start, prm.num_splits,
              prm.BH, prm.Nq, prm.Nk,
              prm.full_mask ? (prm.full_mask_bool ? "bool[B,h,Nq,Nk]" : "additive[B,h,Nq,Nk]")
                            : (prm.mask ? "key[B,Nk]" : "none"),
              prm.causal, prm.seg);
-  fa_fwd_kernel<D, F8, MK><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(prm);
+  fa_fwd_kernel<D, F8, MK, WIN><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(prm);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -62,6 +62,10 @@ int launch_attention(const Params& prm, bool f8, int device, int sm_count, cudaS
       case kMaskF32Scalar: return launch_one<D, true, kMaskF32Scalar>(prm, device, sm_count, stream);
       default: return FA_ERR_UNSUPPORTED;
     }
+  }
+  if (prm.win) {
+    if (prm.mask_kind != kMaskNone) return FA_ERR_UNSUPPORTED;
+    return launch_one<D, false, kMaskNone, true>(prm, device, sm_count, stream);
   }
   switch (prm.mask_kind) {
     case kMaskNone: return launch_one<D, false, kMaskNone>(prm, device, sm_count, stream);

@@ -24,7 +24,7 @@
 #include "fa_attn_launch.h"
 #include "fa_log.h"
 #include "fa_quant.cuh"
-#include "fa_window.cuh"
+#include "fa_window_geom.h"
 #include "fa_diag.cuh"
 
 // Device status word (one per device): 0, or FA_ERR_TIMEOUT once a kernel
@@ -539,88 +539,72 @@ int fa_fwd_split_noalloc(const void* q, const void* k, const void* v, const floa
 }
 
 size_t fa_window_workspace_bytes(int B, int H, int img_h, int img_w, int D) {
-  if (B < 1 || H < 1 || img_h < 1 || img_w < 1 || D < 1) return 0;
-  const size_t rows = (size_t)B * H * img_h * img_w;
-  return 4 * align256(rows * D * 2) + align256(rows * 4);
+  (void)B;
+  (void)H;
+  (void)img_h;
+  (void)img_w;
+  (void)D;
+  return 0;  // the attention kernel gathers and scatters the window rows itself
 }
 
 int fa_fwd_window(const void* q, const void* k, const void* v, void* out, float* lse, int B, int H,
                   int img_h, int img_w, int D, int win_h, int win_w, int shift_h, int shift_w,
                   float scale, void* workspace, size_t workspace_bytes, void* stream) {
+  (void)workspace;  // no scratch is used (see fa.h)
+  (void)workspace_bytes;
   // ---- validation: no CUDA call before this block passes ----
-  if (!q || !k || !v || !out || !lse || !workspace) return FA_ERR_INVALID_ARGUMENT;
+  if (!q || !k || !v || !out || !lse) return FA_ERR_INVALID_ARGUMENT;
   if (B < 1 || H < 1 || img_h < 1 || img_w < 1 || win_h < 1 || win_w < 1)
     return FA_ERR_INVALID_ARGUMENT;
   if (img_h % win_h || img_w % win_w) return FA_ERR_INVALID_ARGUMENT;
   if (D != 32 && D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
   if (!std::isfinite(scale)) return FA_ERR_INVALID_ARGUMENT;
   if ((int64_t)img_h * img_w > INT_MAX) return FA_ERR_INVALID_ARGUMENT;
-  if (!aligned16(workspace) || workspace_bytes < fa_window_workspace_bytes(B, H, img_h, img_w, D))
-    return FA_ERR_INVALID_ARGUMENT;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse))
     return FA_ERR_INVALID_ARGUMENT;
-  const int N = img_h * img_w;
-  const size_t rows = (size_t)B * H * N;
-  const size_t t_bytes = rows * D * 2;
-  const size_t ws_used = fa_window_workspace_bytes(B, H, img_h, img_w, D);
-  if (ranges_overlap(workspace, ws_used, q, t_bytes) || ranges_overlap(workspace, ws_used, k, t_bytes) ||
-      ranges_overlap(workspace, ws_used, v, t_bytes) || ranges_overlap(workspace, ws_used, out, t_bytes) ||
-      ranges_overlap(workspace, ws_used, lse, rows * 4) || ranges_overlap(out, t_bytes, lse, rows * 4))
-    return FA_ERR_INVALID_ARGUMENT;
+  const size_t rows = (size_t)B * H * img_h * img_w;
+  // Windowed rows are indexed in 32 bits (multiply-shift division).
+  if (rows >= (size_t(1) << 31)) return FA_ERR_INVALID_ARGUMENT;
   fa::WindowGeom g{B, H, img_h, img_w, win_h, win_w, 0, 0, D, 1};
   g.shift_h = ((shift_h % img_h) + img_h) % img_h;
   g.shift_w = ((shift_w % img_w) + img_w) % img_w;
   const long long nw = g.windows();
   if ((long long)B * nw > INT_MAX) return FA_ERR_INVALID_ARGUMENT;
-  // Pack windows of up to 64 tokens, as many as fill a 128-row tile, into each
-  // batch entry (a divisor of the window count, so every entry is full).
+  // Pack windows of up to 64 tokens, as many as fill two 128-row tiles, into
+  // each batch entry (a divisor of the window count, so every entry is full):
+  // a work unit then holds two query tiles (both softmax warpgroups busy),
+  // each seeing the keys of its own windows only.
   const int Nw = g.win_tokens();
   if (Nw <= 64) {
-    int pk = 128 / Nw;
+    int pk = 256 / Nw;
     while (pk > 1 && ((long long)B * nw) % pk) --pk;
     g.pack = pk;
   }
-  // Windowed rows are indexed in 32 bits (multiply-shift division).
-  if (rows >= (size_t(1) << 31)) return FA_ERR_INVALID_ARGUMENT;
   g.finish();
-  const long long chunks = (long long)rows * (D / 8);
-  const long long blocks = (chunks + 255) / 256;
-  if (blocks > INT_MAX) return FA_ERR_INVALID_ARGUMENT;
-
-  char* ws = static_cast<char*>(workspace);
-  const size_t t_al = align256(t_bytes);
-  void* qw = ws;
-  void* kw = ws + t_al;
-  void* vw = ws + 2 * t_al;
-  void* ow = ws + 3 * t_al;
-  float* lw = reinterpret_cast<float*>(ws + 4 * t_al);
-  // The batched problem over the gathered windows, validated like fa_fwd's.
+  // The batched problem over the windows, validated like fa_fwd's (its rows
+  // are those of q, k, v, out and lse, in another order).
   const int entries = (int)(B * nw / g.pack), Ne = g.entry_tokens();
   Shape sh;
-  int rc = validate(qw, kw, vw, nullptr, ow, lw, entries, H, Ne, Ne, D, scale, &sh);
+  int rc = validate(q, k, v, nullptr, out, lse, entries, H, Ne, Ne, D, scale, &sh);
   if (rc != FA_OK) return rc;
 
   // ---- set-up (CUDA calls, nothing enqueued yet) ----
   fa::Params prm;
   DeviceState* st = nullptr;
-  rc = setup(qw, kw, vw, nullptr, ow, lw, H, Ne, Ne, D, scale, sh, &prm, &st);
+  rc = setup(q, k, v, nullptr, out, lse, H, Ne, Ne, D, scale, sh, &prm, &st);
   if (rc != FA_OK) return rc;
   prm.seg = g.pack > 1 ? Nw : 0;  // each row sees its own window only
-
-  // ---- enqueue: gather, attention, scatter ----
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  fa::log_launch("fa_window_gather_kernel / fa_window_scatter_kernel grid %lld x 256 threads; "
-             "%d batch entries of %d tokens (%d windows of %dx%d each)",
-             blocks, entries, Ne, g.pack, win_h, win_w);
-  fa::fa_window_gather_kernel<<<(int)blocks, 256, 0, s>>>(
-      static_cast<const uint4*>(q), static_cast<const uint4*>(k), static_cast<const uint4*>(v),
-      static_cast<uint4*>(qw), static_cast<uint4*>(kw), static_cast<uint4*>(vw), g, chunks);
-  if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
-  rc = launch_fwd(prm, *st, D, s);
-  if (rc != FA_OK) return rc;
-  fa::fa_window_scatter_kernel<<<(int)blocks, 256, 0, s>>>(
-      static_cast<const uint4*>(ow), lw, static_cast<uint4*>(out), lse, g, chunks);
-  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  // Window mode: the kernel reads each windowed row of Q, K, V from its grid
+  // position and writes O and LSE back there (no gather or scatter pass).
+  prm.win = 1;
+  prm.wg = g;
+  prm.win_q = static_cast<const __nv_bfloat16*>(q);
+  prm.win_k = static_cast<const __nv_bfloat16*>(k);
+  prm.win_v = static_cast<const __nv_bfloat16*>(v);
+  fa::log_launch("window attention: %d batch entries of %d tokens (%d windows of %dx%d each), "
+                 "rows gathered and scattered by the attention kernel",
+                 entries, Ne, g.pack, win_h, win_w);
+  return launch_fwd(prm, *st, D, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int fa_read_device_status(void* stream, int* status) {

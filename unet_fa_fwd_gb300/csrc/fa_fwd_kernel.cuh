@@ -36,6 +36,7 @@
 #include <cstdint>
 
 #include "fa_fastdiv.h"
+#include "fa_window_geom.h"
 #include "sm100_ptx.cuh"
 
 namespace fa {
@@ -218,6 +219,16 @@ struct Params {
   const float* q_scale;   // F8: [BH][ceil(Nq/128)] e4m3 block scale of Q
   const float* k_scale;   // F8: [BH][nkv] e4m3 block scale of the smoothed K
   const float* lse_corr;  // F8: [BH][Nq] scale * q_i . mean(K), added back to LSE
+  // Window mode (win != 0; the kernel's WIN instantiation): the launch is the
+  // batched problem over windows ([entries][H][entry tokens], see WindowGeom)
+  // but Q, K, V are read from the original [B][H][tokens][D] tensors and O,
+  // LSE written to the original [B][H][tokens] rows, each windowed row through
+  // WindowGeom::source_row.
+  int win;
+  WindowGeom wg;
+  const __nv_bfloat16* win_q;
+  const __nv_bfloat16* win_k;
+  const __nv_bfloat16* win_v;
   // -- TMA descriptors (each 64-byte aligned) --
   CUtensorMap tm_q;  // [BH][Nq][D] bf16 (e4m3 for the F8 kernel)
   CUtensorMap tm_k;  // [BH][Nk][D]
@@ -662,10 +673,44 @@ __device__ __forceinline__ float general_pass1_staged(uint32_t tS, const uint8_t
   return mx;
 }
 
+// Window mode: one 128-row bf16 tile, windowed rows row0 .. row0 + 127 (rows
+// from nvalid on repeat row nvalid - 1, whose results are discarded), copied
+// by the whole warp from the original tensor `src` with cp.async (16 bytes
+// per lane per instruction, consecutive lanes on consecutive pieces of a
+// row) into the layout a TMA tile load writes: 128-row chunk blocks of SW-byte
+// rows, 16-byte piece c of row r at piece c ^ (r mod 8) (128-byte swizzle) or
+// c ^ ((r / 2) mod 4) (64-byte swizzle).  Each lane maps four rows (lane,
+// lane + 32, ...) and the others take them by shuffle.
+template <int D>
+__device__ __forceinline__ void window_tile(const WindowGeom& g, const __nv_bfloat16* src,
+                                            uint32_t row0, int nvalid, uint32_t dst, uint32_t lane) {
+  constexpr int SW = (D >= 64) ? 128 : 64;
+  constexpr int CPR = D / 8;      // 16-byte pieces per row
+  constexpr int CPB = SW / 16;    // pieces per swizzled row of a chunk block
+  constexpr int RPI = 32 / CPR;   // rows per instruction
+  uint32_t srow[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int r = k * 32 + (int)lane;
+    srow[k] = (uint32_t)g.source_row(row0 + (uint32_t)(r < nvalid ? r : nvalid - 1));
+  }
+#pragma unroll
+  for (int k = 0; k < 128 / RPI; ++k) {
+    const int r = k * RPI + (int)lane / CPR;
+    const int c = (int)lane % CPR;
+    const uint32_t sr = __shfl_sync(0xffffffffu, srow[(k * RPI) / 32], r % 32);
+    const __nv_bfloat16* gp = src + (size_t)sr * D + c * 8;
+    const int swz = SW == 128 ? (r & 7) : ((r >> 1) & 3);
+    const uint32_t so = dst + (uint32_t)((c / CPB) * (128 * SW) + r * SW + (((c % CPB) ^ swz) << 4));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(so), "l"(gp) : "memory");
+  }
+}
+
 // MK: how the general softmax path reads mask values (kMask*).  Each kind is
 // its own instantiation, so a launch carries only the mask code it runs (the
-// kernel's speed is sensitive to its instruction footprint).
-template <int D, bool F8, int MK>
+// kernel's speed is sensitive to its instruction footprint).  WIN: window mode
+// (rows gathered and scattered through the window map; Params::win).
+template <int D, bool F8, int MK, bool WIN>
 __global__ void __launch_bounds__(Cfg<D, F8, MK>::THREADS, 1)
     fa_fwd_kernel(const __grid_constant__ Params p) {
   using C = Cfg<D, F8, MK>;
@@ -732,7 +777,79 @@ __global__ void __launch_bounds__(Cfg<D, F8, MK>::THREADS, 1)
   ptx::setmaxnreg_dec<C::REGS_OTHER>();
   if (warp == 8) {
     // ------------------------------------------------------------ producer --
-    if (lane == 0) {
+    if constexpr (WIN) {
+      // Window mode: the whole warp gathers tiles with cp.async.  A tile's
+      // copies form one group; once at most kInFlight later groups are
+      // pending it has landed, and each lane fences its writes for the tensor
+      // cores (async proxy) before lane 0 arrives on the tile's barrier.
+      // Before waiting for the Q buffer every group is flushed (the MMA needs
+      // all of the last unit's K tiles to release Q).
+      constexpr int kInFlight = 2;
+      uint32_t pd0 = 0, pd1 = 0, pd2 = 0;  // barriers of pending groups, oldest first
+      int np = 0;
+      auto arrive_oldest = [&]() {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(pd0);
+        pd0 = pd1;
+        pd1 = pd2;
+        --np;
+      };
+      auto commit = [&](uint32_t bar) {
+        asm volatile("cp.async.commit_group;" ::: "memory");
+        if (np == 0) pd0 = bar; else if (np == 1) pd1 = bar; else pd2 = bar;
+        ++np;
+        if (np > kInFlight) {
+          asm volatile("cp.async.wait_group %0;" ::"n"(kInFlight) : "memory");
+          arrive_oldest();
+        }
+      };
+      auto flush = [&]() {
+        asm volatile("cp.async.wait_all;" ::: "memory");
+        while (np > 0) arrive_oldest();
+      };
+      const uint32_t sq = ptx::smem_u32(sQ), sring = ptx::smem_u32(sRing);
+      uint32_t it = 0, uc = 0;
+      bool ok = true;
+      for (int ui = 0, u = snake_unit(0); u < p.num_units && ok; u = snake_unit(++ui), ++uc) {
+        const Unit un = decode_unit(p, u);
+        const int bh = un.bh, q0 = un.q0;
+        flush();
+        ok = bounded_wait_warp(ptx::smem_u32(&bars->q_empty), (uc & 1) ^ 1, bars, p.timeout_ns, p.status);
+        if (!ok) break;
+        if (!fa_check(p, bars, unit_in_bounds(p, un), kCheckUnit, u, un.bh)) {
+          ok = false;
+          break;
+        }
+#ifdef FA_DEBUG
+        if (lane == 0) {
+          bars->dbg_unit[0] = u;
+          bars->dbg_unit[1] = bh;
+          bars->dbg_unit[2] = q0;
+        }
+#endif
+        for (int t = 0; t < un.nq; ++t)
+          window_tile<D>(p.wg, p.win_q, (uint32_t)(bh * p.Nq + q0 + t * 128), p.Nq - (q0 + t * 128),
+                         sq + t * C::QK_TILE_BYTES, lane);
+        commit(ptx::smem_u32(&bars->q_full));
+        for (int j = 0; j < un.ntiles && ok; ++j) {
+          const int kb = (un.tile0 + j) * 128;
+          for (int kv = 0; kv < 2; ++kv, ++it) {
+            const uint32_t s = it % C::STAGES;
+            const uint32_t ph = (it / C::STAGES) & 1;
+            ok = bounded_wait_warp(ptx::smem_u32(&bars->kv_empty[s]), ph ^ 1, bars, p.timeout_ns, p.status);
+            if (!ok) break;
+            window_tile<D>(p.wg, kv ? p.win_v : p.win_k, (uint32_t)(bh * p.Nk + kb), p.Nk - kb,
+                           sring + s * C::TILE_BYTES, lane);
+            commit(ptx::smem_u32(&bars->kv_full[s]));
+          }
+        }
+      }
+      if (ok)
+        flush();
+      else
+        asm volatile("cp.async.wait_all;" ::: "memory");  // nothing lands after the CTA ends
+    } else if (lane == 0) {
       ptx::tma_prefetch_desc(&p.tm_q);
       ptx::tma_prefetch_desc(&p.tm_k);
       ptx::tma_prefetch_desc(&p.tm_v);
@@ -1442,6 +1559,12 @@ __global__ void __launch_bounds__(Cfg<D, F8, MK>::THREADS, 1)
       ptx::tc_fence_after_sync();
       const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
       const bool valid_row = qrow < p.Nq;
+      // Output row of query row r of this head (window mode: its grid position).
+      auto out_row = [&](int r) -> size_t {
+        const size_t wr = (size_t)bh * p.Nq + r;
+        if constexpr (WIN) return (size_t)p.wg.source_row((uint32_t)wr);
+        return wr;
+      };
       constexpr float kLn2 = 0.6931471805599453f;
       float row_lse = (l > 0.f) ? (m + __log2f(l)) * kLn2 : -INFINITY;
       if constexpr (F8) {
@@ -1486,11 +1609,11 @@ __global__ void __launch_bounds__(Cfg<D, F8, MK>::THREADS, 1)
 #else
           if (orow < p.Nq)
 #endif
-            *reinterpret_cast<uint4*>(p.out + ((size_t)bh * p.Nq + orow) * D + c * 8) = v;
+            *reinterpret_cast<uint4*>(p.out + out_row(orow) * D + c * 8) = v;
         }
         __syncwarp();  // the buffer is written again in the next unit
         if (valid_row && fa_check(p, bars, bh < p.BH, kCheckStore, (long long)bh * p.Nq + qrow, -1))
-          p.lse[(size_t)bh * p.Nq + qrow] = row_lse;
+          p.lse[out_row(qrow)] = row_lse;
       } else if (p.part_o == nullptr) {
         // Coalesced stores: thread = row in tensor memory, so each 32-column
         // chunk (16 bf16 pairs per row) is transposed across the warp with
@@ -1529,12 +1652,12 @@ __global__ void __launch_bounds__(Cfg<D, F8, MK>::THREADS, 1)
 #else
             if (orow < p.Nq)
 #endif
-              *reinterpret_cast<uint4*>(p.out + ((size_t)bh * p.Nq + orow) * D + cb + piece * 8) =
+              *reinterpret_cast<uint4*>(p.out + out_row(orow) * D + cb + piece * 8) =
                   make_uint4(w[0], w[1], w[2], w[3]);
           }
         }
         if (valid_row && fa_check(p, bars, bh < p.BH, kCheckStore, (long long)bh * p.Nq + qrow, -1))
-          p.lse[(size_t)bh * p.Nq + qrow] = row_lse;
+          p.lse[out_row(qrow)] = row_lse;
       } else {
         // Split mode: this key range's normalised O (fp32) and its LSE, merged
         // by fa_merge_kernel.
