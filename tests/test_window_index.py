@@ -1,4 +1,4 @@
-"""The window gather/scatter's index map (multiply-shift division, fa_window_geom.h)
+"""The window map of the attention kernel's window mode (multiply-shift division, fa_window_geom.h)
 agrees with its division-by-division definition: compiled with the host C++
 compiler and run over every row of a set of window geometries, packs and shifts."""
 import os

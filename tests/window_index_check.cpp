@@ -1,8 +1,8 @@
-// The window gather/scatter's index map (WindowGeom::source_row, multiply-shift
+// The window map of the attention kernel's window mode (WindowGeom::source_row, multiply-shift
 // division by the launch's sizes) agrees with its division-by-division
 // definition (source_token and the windowed layout [entries, H, pack *
 // win_tokens]) for every row of a set of geometries: square and rectangular
-// windows, packs of 1..16 windows per entry, cyclic shifts including wrap-around.
+// windows, packs of 1..64 windows per entry, cyclic shifts including wrap-around.
 // Prints "ok" or the first mismatch.
 #include <cstdio>
 #include <cstdint>
@@ -48,7 +48,7 @@ int main() {
             const int nw = (img_h / win_h) * (img_w / win_w);
             // every pack that divides the window count of the batch (the host
             // picks one of these)
-            for (int pack = 1; pack <= 16; ++pack) {
+            for (int pack = 1; pack <= 64; ++pack) {
               if ((B * nw) % pack) continue;
               if (check(B, H, img_h, img_w, win_h, win_w, s[0], s[1], D, pack)) return 1;
             }

@@ -1,6 +1,8 @@
 // fa_window_geom.h — the window / shifted-window geometry shared by the
-// gather and scatter kernels and the host set-up (plain C++ on the host, so the
-// index map is checked there against its division-by-division definition).
+// attention kernel's window mode (its producer gathers Q/K/V rows and its
+// epilogue writes O/LSE rows through source_row) and the host set-up (plain
+// C++ on the host, so the index map is checked there against its
+// division-by-division definition).
 #pragma once
 
 #include <cstdint>
