@@ -412,7 +412,7 @@ def bench_native(args, world, rank, local):
             hl.copy_(dl, non_blocking=True)
             out_done[b].record(s_out)
 
-    e2e_steps = max(5, args.steps // 20) if variant == "fwd" else 0
+    e2e_steps = max(10, args.steps // 10) if variant == "fwd" else 0
     e2e_secs = 0.0
     if e2e_steps:
         for i in range(2):
