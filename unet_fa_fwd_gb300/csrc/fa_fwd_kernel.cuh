@@ -267,13 +267,24 @@ __device__ __forceinline__ Unit decode_unit(const Params& p, int u) {
     r.nq = 1;
   } else if (p.causal) {
     // Causal (one key range): a pair's work grows with its query position, so
-    // units run heaviest first across all heads (pair index descending, heads
-    // inner); dealt to the CTAs in snake order (snake_unit) this keeps the
-    // CTAs' totals close, and the units of a head still start together.
-    const uint32_t k = p.div_bh.div((uint32_t)u);
+    // units run heaviest first.  When a head has fewer pairs than the grid has
+    // CTAs, across all heads (pair index descending, heads inner): each round
+    // then holds units of equal weight, and dealt to the CTAs in snake order
+    // (snake_unit) the CTAs' totals stay close.  When a head has at least a
+    // round of pairs, head by head (heaviest first within each head): the
+    // CTAs running together then sweep one head's keys, which stay in L2,
+    // where heads inner would stream every head's K/V at once; the snake
+    // order pairs each round's heavy end with the next round's light end.
     r.split = 0;
-    r.bh = u - (int)k * p.BH;
-    r.q0 = (int)(upb - 1 - k) * 256;
+    if (p.units_per_bh >= (int)gridDim.x) {
+      const uint32_t k = p.div_upb.div((uint32_t)u);
+      r.bh = (int)k;
+      r.q0 = (int)(upb - 1 - ((uint32_t)u - k * upb)) * 256;
+    } else {
+      const uint32_t k = p.div_bh.div((uint32_t)u);
+      r.bh = u - (int)k * p.BH;
+      r.q0 = (int)(upb - 1 - k) * 256;
+    }
     r.nq = (r.q0 + 128 < p.Nq) ? 2 : 1;
   } else {
     uint32_t rest = (uint32_t)u;
