@@ -75,3 +75,14 @@ def test_window_is_one_launch_without_workspace(monkeypatch, capfd):
     assert fa.read_device_status() == 0
     kernels = [ln for ln in capfd.readouterr().err.splitlines() if ln.startswith("[fa] fa_")]
     assert len(kernels) == 1 and "window rows" in kernels[0], kernels
+
+
+def test_window_bitwise_deterministic():
+    """Two runs of the same shifted-window launch give the same bits."""
+    inp = workloads.make_inputs("sd_self", device="cuda", B=2, H=2)
+    args = (inp["q"], inp["k"], inp["v"], 64, 64, 8, 8, 4, 4)
+    o1, l1 = fa.fwd_window(*args, scale=inp["scale"])
+    o2, l2 = fa.fwd_window(*args, scale=inp["scale"])
+    torch.cuda.synchronize()
+    assert fa.read_device_status() == 0
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
