@@ -106,17 +106,18 @@ def test_causal_flux_1024_full_size():
     compare(out, lse, o_ref, l_ref, rows=rows, label="causal flux_1024")
 
 
-def test_causal_long_heads_run_head_by_head():
+@pytest.mark.parametrize("D", [64, 128])
+def test_causal_long_heads_run_head_by_head(D):
     """Causal with more query pairs per head than the grid has CTAs: units run
     head by head, heaviest first within a head (rows sampled from every region
     of the triangle, the ragged last tile included)."""
     G = torch.cuda.get_device_properties(0).multi_processor_count
     Nq = 256 * (G + 5) - 100
-    inp = _inputs(64, 1, 2, Nq, Nq)
+    inp = _inputs(D, 1, 2, Nq, Nq)
     rows = workloads.sample_rows(Nq, 2, 96, seed=4)  # rows 0 and Nq - 1 included
     out, lse = _run(inp, causal=True)
     o_ref, l_ref = _oracle(inp, causal=True, rows=rows)
-    compare(out, lse, o_ref, l_ref, rows=rows, label="causal long heads")
+    compare(out, lse, o_ref, l_ref, rows=rows, label=f"causal long heads D{D}")
 
 
 def test_mask_validation():
