@@ -81,6 +81,22 @@ def test_bool_mask(D, causal, Nk):
     compare(out, lse, o_ref, l_ref, label=f"bool D{D} causal{causal} Nk{Nk}")
 
 
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("Nq,Nk", [(300, 512), (513, 260), (129, 1000)])
+def test_key_padding_with_causal(D, Nq, Nk):
+    """Key-padding mask and the causal triangle together: Nk a multiple of 4
+    (the mask values come from the lanes' shuffled loads) with valid lengths
+    that cut blocks, and one batch entry whose padding covers whole blocks."""
+    inp = _inputs(D, 2, 2, Nq, Nk)
+    g = torch.Generator(device="cuda").manual_seed(9)
+    km = torch.randn(2, Nk, generator=g, device="cuda")
+    km[0, Nk - Nk // 3:] = float("-inf")
+    km[1, 130:300] = float("-inf")
+    out, lse = _run(inp, key_mask=km, causal=True)
+    o_ref, l_ref = _oracle(inp, key_mask=km, causal=True)
+    compare(out, lse, o_ref, l_ref, label=f"key mask + causal D{D} {Nq}x{Nk}")
+
+
 def test_key_padding_through_ex_matches_fa_fwd():
     inp = workloads.make_inputs("sd_cross", device="cuda")
     o1, l1 = _run(inp, key_mask=inp["mask"])

@@ -30,6 +30,7 @@ def _device():
     ((16, 16), (4, 4), (2, 2)),          # 16-token windows: 8 per 128-row batch entry
     ((8, 8), (2, 2), (1, 1)),            # 4-token windows: 32 per entry
     ((12, 8), (4, 4), (0, 0)),           # 12 windows in all: packing falls back to 6 per entry
+    ((32, 32), (8, 8), (3, 5)),          # 16 windows of 64 per image, 4 per entry, odd shifts
 ])
 def test_window_parity(D, img, win, shift):
     base = {32: "page_example", 64: "sd_self", 128: "flux_1024"}[D]
